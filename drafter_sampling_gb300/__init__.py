@@ -1,0 +1,247 @@
+"""drafter_sampling_gb300: VocabTrim drafting and speculative verification on
+one GB300 GPU (sm_103a).
+
+Thin Python binding over libvt.so (include/vt.h).  Each function below has
+the name of the C entry point it calls and only marshals arguments: it checks
+tensor devices, dtypes and shapes, allocates outputs and workspace with
+PyTorch, and passes raw device pointers and the current CUDA stream.  Every
+step of the computation runs in the library's CUDA kernels.
+
+bf16 tensors may be passed as torch.bfloat16 or as int16/uint16 bit patterns.
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
+                   VT_DEV_DUPLICATE_ID, VT_DEV_NONFINITE, VT_DEV_ZERO_RESIDUAL, VT_F32,
+                   VtError)
+
+__all__ = ["vt_calibrate_topk", "vt_trim_head", "vt_draft_logits", "vt_draft_step",
+           "vt_verify", "workspace_bytes", "VtError", "lib"]
+
+
+def lib():
+    """The loaded ctypes library (raises if libvt.so is not built)."""
+    return _lib.load()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t, name, dtypes, dim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got {t.dim()}")
+    return t
+
+
+def _bf16_dtypes():
+    torch = _torch()
+    return (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _ws(nbytes, device):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def workspace_bytes(kind: str, **kw) -> int:
+    L = lib()
+    if kind == "calibrate":
+        return L.vt_calibrate_topk_workspace_bytes(kw["n"], kw["V"], kw["K"])
+    if kind == "draft":
+        return L.vt_draft_workspace_bytes(kw["B"], kw["H"], kw["K"])
+    if kind == "verify":
+        return L.vt_verify_workspace_bytes(kw["B"], kw["gamma"], kw["V"], kw["K"])
+    raise ValueError(kind)
+
+
+def vt_calibrate_topk(ids, V: int, K: int, counts=None, topk_ids=None, dev_status=None,
+                      workspace=None, stream=None):
+    """Token histogram and Top-K (count desc, id asc) of int32 ids.
+
+    Returns (counts uint32-as-int32 [V], topk_ids int32 [K], dev_status int32 [1]).
+    """
+    torch = _torch()
+    _dev(ids, "ids", (torch.int32,), 1)
+    dev = ids.device
+    n = ids.numel()
+    if counts is None:
+        counts = torch.empty(V, dtype=torch.int32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty(K, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    _dev(counts, "counts", (torch.int32, torch.uint32), 1)
+    _dev(topk_ids, "topk_ids", (torch.int32,), 1)
+    if counts.numel() != V or topk_ids.numel() != K:
+        raise ValueError("counts must have V elements and topk_ids K elements")
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_calibrate_topk_workspace_bytes(n, V, K), dev)
+    st = L.vt_calibrate_topk(ids.data_ptr(), n, V, K, counts.data_ptr(), topk_ids.data_ptr(),
+                             dev_status.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                             _stream_ptr(stream))
+    _lib.check("vt_calibrate_topk", st)
+    return counts, topk_ids, dev_status
+
+
+def vt_trim_head(W, topk_ids, W_trim=None, trim_ids=None, inv_map=None, dev_status=None,
+                 stream=None):
+    """W_trim = W[sorted(topk_ids)], trim_ids (ascending) and inv_map.
+
+    Returns (W_trim [K,H] same dtype as W, trim_ids int32 [K], inv_map int32 [V], dev_status).
+    """
+    torch = _torch()
+    _dev(W, "W", _bf16_dtypes(), 2)
+    _dev(topk_ids, "topk_ids", (torch.int32,), 1)
+    V, H = W.shape
+    K = topk_ids.numel()
+    dev = W.device
+    if W_trim is None:
+        W_trim = torch.empty((K, H), dtype=W.dtype, device=dev)
+    if trim_ids is None:
+        trim_ids = torch.empty(K, dtype=torch.int32, device=dev)
+    if inv_map is None:
+        inv_map = torch.empty(V, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
+    if tuple(W_trim.shape) != (K, H) or trim_ids.numel() != K or inv_map.numel() != V:
+        raise ValueError("output shapes do not match (K, H), K and V")
+    st = lib().vt_trim_head(W.data_ptr(), V, H, topk_ids.data_ptr(), K, W_trim.data_ptr(),
+                            trim_ids.data_ptr(), inv_map.data_ptr(), dev_status.data_ptr(),
+                            _stream_ptr(stream))
+    _lib.check("vt_trim_head", st)
+    return W_trim, trim_ids, inv_map, dev_status
+
+
+def vt_draft_logits(hidden, W_trim, temperature: float = 1.0, logits=None, workspace=None,
+                    stream=None):
+    """logits [B, K] fp32 = hidden @ W_trim^T / T."""
+    torch = _torch()
+    _dev(hidden, "hidden", _bf16_dtypes(), 2)
+    _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
+    B, H = hidden.shape
+    K, H2 = W_trim.shape
+    if H2 != H:
+        raise ValueError("hidden and W_trim disagree on H")
+    if logits is None:
+        logits = torch.empty((B, K), dtype=torch.float32, device=hidden.device)
+    if logits.dim() != 2 or logits.shape[0] != B or logits.stride(1) != 1 or logits.shape[1] < K:
+        raise ValueError("logits must be [B, >=K] with unit inner stride")
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_draft_workspace_bytes(B, H, K), hidden.device)
+    st = L.vt_draft_logits(hidden.data_ptr(), B, H, W_trim.data_ptr(), K, float(temperature),
+                           logits.data_ptr(), logits.stride(0), workspace.data_ptr(),
+                           workspace.numel(), _stream_ptr(stream))
+    _lib.check("vt_draft_logits", st)
+    return logits
+
+
+def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, q=None,
+                  tokens=None, dev_status=None, workspace=None, stream=None):
+    """One drafting step; returns (q [B, K] view, tokens int32 [B], dev_status).
+
+    ``q`` may be a strided view such as q_all[:, pos, :] of a contiguous
+    [B, gamma, K] tensor (unit inner stride).
+    """
+    torch = _torch()
+    _dev(hidden, "hidden", _bf16_dtypes(), 2)
+    _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
+    _dev(trim_ids, "trim_ids", (torch.int32,), 1)
+    _dev(uniforms, "uniforms", (torch.float32,), 1)
+    B, H = hidden.shape
+    K = W_trim.shape[0]
+    dev = hidden.device
+    if q is None:
+        q = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if q.dim() != 2 or q.shape[0] != B or q.shape[1] != K or q.stride(1) != 1:
+        raise ValueError("q must be [B, K] with unit inner stride")
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    if uniforms.numel() != B or trim_ids.numel() != K:
+        raise ValueError("uniforms must have B and trim_ids K elements")
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_draft_workspace_bytes(B, H, K), dev)
+    st = L.vt_draft_step(hidden.data_ptr(), B, H, W_trim.data_ptr(), trim_ids.data_ptr(), K,
+                         uniforms.data_ptr(), float(temperature), q.data_ptr(), q.stride(0),
+                         tokens.data_ptr(), dev_status.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), _stream_ptr(stream))
+    _lib.check("vt_draft_step", st)
+    return q, tokens, dev_status
+
+
+def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
+              temperature: float = 1.0, out_tokens=None, out_num_accepted=None,
+              out_accept_prob=None, dev_status=None, workspace=None, stream=None,
+              want_accept_prob: bool = True):
+    """Modified rejection sampling over a batch of drafted blocks.
+
+    target_logits [B, gamma+1, V] float32 or bf16; q [B, gamma, K] float32.
+    Returns (out_tokens [B, gamma+1], out_num_accepted [B], out_accept_prob
+    [B, gamma] or None, dev_status [1]).
+    """
+    torch = _torch()
+    if target_logits.dtype == torch.float32:
+        dt = VT_F32
+    elif target_logits.dtype in _bf16_dtypes():
+        dt = VT_BF16
+    else:
+        raise TypeError("target_logits must be float32 or bf16")
+    _dev(target_logits, "target_logits", (target_logits.dtype,), 3)
+    _dev(q, "q", (torch.float32,), 3)
+    _dev(inv_map, "inv_map", (torch.int32,), 1)
+    _dev(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    _dev(u_accept, "u_accept", (torch.float32,), 2)
+    _dev(u_resample, "u_resample", (torch.float32,), 2)
+    B, R, V = target_logits.shape
+    gamma = R - 1
+    K = q.shape[2]
+    if tuple(q.shape[:2]) != (B, gamma) or tuple(draft_tokens.shape) != (B, gamma):
+        raise ValueError("q / draft_tokens shapes do not match target_logits")
+    if tuple(u_accept.shape) != (B, gamma) or tuple(u_resample.shape) != (B, R):
+        raise ValueError("uniform shapes do not match")
+    if inv_map.numel() != V:
+        raise ValueError("inv_map must have V entries")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, R), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_accept_prob is None and want_accept_prob:
+        out_accept_prob = torch.empty((B, gamma), dtype=torch.float32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_verify_workspace_bytes(B, gamma, V, K), dev)
+    st = L.vt_verify(target_logits.data_ptr(), dt, B, gamma, V, q.data_ptr(), inv_map.data_ptr(),
+                     K, draft_tokens.data_ptr(), u_accept.data_ptr(), u_resample.data_ptr(),
+                     float(temperature), out_tokens.data_ptr(), out_num_accepted.data_ptr(),
+                     out_accept_prob.data_ptr() if out_accept_prob is not None else None,
+                     dev_status.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                     _stream_ptr(stream))
+    _lib.check("vt_verify", st)
+    return out_tokens, out_num_accepted, out_accept_prob, dev_status

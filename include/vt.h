@@ -1,0 +1,202 @@
+/*
+ * vt.h - C ABI of libvt: the data-parallel hot path of drafter-based
+ * speculative decoding with a VocabTrim-trimmed drafter head, on one GPU.
+ *
+ * Pages that define the operations (cited by title and section):
+ *  [VT]  "VocabTrim: Vocabulary Pruning for Efficient Speculative Decoding in
+ *        LLMs" (arXiv 2506.22694): section 3, Algorithm 1 and eq. (1);
+ *        Appendix C.1, Algorithm 2.
+ *  [GL]  "Speculative decoding" (SelfMadeQuant glossary): sections "Propose a
+ *        block, keep a prefix", "Why a rejection needs a special draw",
+ *        "Distributional exactness has conditions".
+ *  [NB]  "A rejection rule keeps speculative decoding's output exact" (the
+ *        nightly build): sections "A target and a draft small enough to print
+ *        in full" (the inverse-CDF sampler) and "Extending the rule from one
+ *        token to a drafted run" (block verification and the bonus draw).
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no pointer after the call returns and frees nothing.
+ *  - bf16 arrays are passed as uint16_t bit patterns (bfloat16).
+ *  - Arrays are dense, row-major, with the strides stated per argument.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is asynchronous on `stream`; the return code reports only what the
+ *    host can check (arguments, workspace size, launch errors).
+ *  - Problems found in the DATA are reported by the device in *dev_status as
+ *    a bit mask of VT_DEV_* flags; the call zeroes *dev_status first.  Read
+ *    it after synchronising the stream.  When a VT_DEV_BAD_* or
+ *    VT_DEV_NONFINITE bit is set, the affected outputs are unspecified.
+ *  - `workspace` is caller-allocated device scratch of at least the size the
+ *    matching *_workspace_bytes() query returns, 256-byte aligned.  Its
+ *    contents need not be initialised.  Two calls that are in flight at the
+ *    same time must not share a workspace.
+ *  - The library holds no random number generator: every uniform the method
+ *    draws is an explicit input in [0, 1).
+ *  - Device code targets sm_103a only.
+ */
+#ifndef VT_H_
+#define VT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+enum {
+  VT_OK = 0,
+  VT_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad temperature ...  */
+  VT_ERR_UNSUPPORTED = -2,  /* valid request this build does not implement */
+  VT_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed         */
+  VT_ERR_BAD_INPUT = -4,    /* reserved for host-detected bad data          */
+  VT_ERR_WORKSPACE = -5     /* workspace missing, too small or misaligned  */
+};
+
+/* Element types of target logits. */
+enum { VT_F32 = 0, VT_BF16 = 1 };
+
+/* Bits the device sets in *dev_status. */
+enum {
+  VT_DEV_BAD_ID = 1,         /* token id outside [0, V)                        */
+  VT_DEV_DUPLICATE_ID = 2,   /* the same id appears twice in a top-K list      */
+  VT_DEV_BAD_DRAFT = 4,      /* drafted token out of range, not trimmed, or
+                                q(x) <= 0 at a drafted token                    */
+  VT_DEV_NONFINITE = 8,      /* NaN/Inf reached a softmax normaliser           */
+  VT_DEV_ZERO_RESIDUAL = 16  /* informational: residual mass was zero at a
+                                rejection; that draw used p instead            */
+};
+
+/* Human-readable text for a return code. Never NULL. */
+const char* vt_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+int vt_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * Calibration: token-frequency histogram and Top-K selection.
+ * [VT] Algorithm 1 (a counter c in N^|V| starts at zero and is incremented
+ * once per token occurrence) and eq. (1) Top-K(c, k).  Ties in the count are
+ * broken by the lower token id.
+ *
+ *  ids       int32 [n]       calibration token ids, each in [0, V)
+ *  n         number of ids (>= 0)
+ *  V         vocabulary size (1 <= V <= 2^30)
+ *  K         number of ids kept (1 <= K <= V)
+ *  counts    uint32 [V]      out: c[t] = occurrences of t (ids outside
+ *                            [0, V) are skipped and flag VT_DEV_BAD_ID)
+ *  topk_ids  int32 [K]       out: the K ids ranked by (count desc, id asc)
+ *  dev_status int32 [1]      out: VT_DEV_* bits
+ * Counts are exact (bit-identical to a sequential count) for n < 2^32.
+ * ---------------------------------------------------------------------- */
+size_t vt_calibrate_topk_workspace_bytes(int64_t n, int32_t V, int32_t K);
+int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
+                      uint32_t* counts, int32_t* topk_ids, int32_t* dev_status,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Trimmed LM head.  [VT] eq. (1): W^Trim = W[Top-K(c,k), :]; Algorithm 2's
+ * token index mapper T_{d->t} (trimmed index -> target id) and its inverse.
+ * Rows are kept in ascending target-id order.
+ *
+ *  W         bf16 [V, H]     full LM head, row stride H
+ *  topk_ids  int32 [K]       K distinct ids in [0, V), any order
+ *  W_trim    bf16 [K, H]     out: W_trim[j, :] = W[trim_ids[j], :] bit for bit
+ *  trim_ids  int32 [K]       out: the selected ids, ascending (T_{d->t})
+ *  inv_map   int32 [V]       out: inv_map[trim_ids[j]] = j, -1 elsewhere
+ *  dev_status int32 [1]      out: VT_DEV_BAD_ID / VT_DEV_DUPLICATE_ID
+ * Needs no workspace.
+ * ---------------------------------------------------------------------- */
+int vt_trim_head(const uint16_t* W, int32_t V, int32_t H,
+                 const int32_t* topk_ids, int32_t K,
+                 uint16_t* W_trim, int32_t* trim_ids, int32_t* inv_map,
+                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Drafter logits through the trimmed head.  [VT] Algorithm 2, drafting
+ * (the trimmed drafter scores only the K trimmed ids); temperature divides
+ * the logits ([GL] "Distributional exactness has conditions").
+ *
+ *  hidden    bf16 [B, H]     drafter hidden states, row stride H
+ *  W_trim    bf16 [K, H]     trimmed head
+ *  logits    f32  [B, ld_logits] out: logits[b, j] = (sum_h hidden[b,h] *
+ *            W_trim[j,h]) / T, accumulated in fp32; ld_logits >= K
+ * 1 <= B <= 4096, 1 <= H <= 65536, 1 <= K; T finite and > 0.
+ * ---------------------------------------------------------------------- */
+size_t vt_draft_workspace_bytes(int32_t B, int32_t H, int32_t K);
+int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
+                    const uint16_t* W_trim, int32_t K, float temperature,
+                    float* logits, int64_t ld_logits,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * One drafting step.  [VT] Algorithm 2, drafting: logits over the trimmed
+ * vocabulary, q = softmax(logits / T), one categorical draw per row, mapped
+ * to a target id by trim_ids.  The draw is the inverse CDF of [NB] with a
+ * strict comparison: the smallest trimmed index j whose running sum of q
+ * (ascending j, i.e. ascending target id) exceeds u_b * sum(q); if rounding
+ * leaves none, the last j with q_j > 0.
+ *
+ *  hidden    bf16 [B, H]     drafter hidden states
+ *  W_trim    bf16 [K, H]     trimmed head
+ *  trim_ids  int32 [K]       trimmed index -> target id
+ *  uniforms  f32  [B]        one uniform in [0,1) per row
+ *  q         f32  [B, ldq]   out: q[b, j] for j < K (ldq >= K; pass
+ *                            ldq = gamma*K and q + pos*K to fill position
+ *                            `pos` of a [B, gamma, K] tensor)
+ *  tokens    int32 [B]       out: drafted target ids
+ *  dev_status int32 [1]      out: VT_DEV_NONFINITE
+ * ---------------------------------------------------------------------- */
+int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
+                  const uint16_t* W_trim, const int32_t* trim_ids, int32_t K,
+                  const float* uniforms, float temperature,
+                  float* q, int64_t ldq, int32_t* tokens, int32_t* dev_status,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Batched block verification by modified rejection sampling.
+ * [GL] "Why a rejection needs a special draw": accept a drafted x with
+ * probability a(x) = min(1, p(x)/q(x)); on rejection draw from
+ * norm(max(p - q, 0)) over the full vocabulary.  [GL] "Propose a block, keep
+ * a prefix" and [NB] "Extending the rule ...": test left to right, keep the
+ * accepted prefix, replace the first rejected token with the residual draw
+ * made from THAT position's p and q, discard the rest; if all gamma drafts
+ * are accepted, draw a bonus token from p at position gamma.
+ * p_i = softmax(logits[b, i, :] / T) over all V ids; q_i is zero outside the
+ * trimmed vocabulary.  Accept iff u_accept[b,i] < a(x).  Every draw is the
+ * strict inverse CDF in ascending token-id order (see vt_draft_step).
+ *
+ *  target_logits  [B, gamma+1, V] of logits_dtype (VT_F32 or VT_BF16)
+ *  q         f32  [B, gamma, K]   drafter probabilities over trimmed ids
+ *  inv_map   int32 [V]            target id -> trimmed index, -1 if absent
+ *  draft_tokens int32 [B, gamma]  drafted target ids
+ *  u_accept  f32  [B, gamma]      accept uniforms
+ *  u_resample f32 [B, gamma+1]    uniform of the residual (or bonus) draw;
+ *                                 entry n_b is used
+ *  temperature                    T > 0, the T that produced q
+ *  out_tokens int32 [B, gamma+1]  out: draft[0..n_b-1], then the drawn
+ *                                 token, then -1
+ *  out_num_accepted int32 [B]     out: n_b in [0, gamma]
+ *  out_accept_prob f32 [B, gamma] out, may be NULL: a(x) at each tested
+ *                                 position (0..min(n_b, gamma-1)); NaN at
+ *                                 positions after the first rejection
+ *  dev_status int32 [1]           out: VT_DEV_BAD_DRAFT, VT_DEV_NONFINITE,
+ *                                 VT_DEV_ZERO_RESIDUAL
+ * 1 <= gamma <= 64, 1 <= B, 1 <= K <= V.
+ * ---------------------------------------------------------------------- */
+size_t vt_verify_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t K);
+int vt_verify(const void* target_logits, int32_t logits_dtype,
+              int32_t B, int32_t gamma, int32_t V,
+              const float* q, const int32_t* inv_map, int32_t K,
+              const int32_t* draft_tokens, const float* u_accept,
+              const float* u_resample, float temperature,
+              int32_t* out_tokens, int32_t* out_num_accepted,
+              float* out_accept_prob, int32_t* dev_status,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VT_H_ */

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry
+point include/vt.h declares.  Only calls that touch no device are made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from drafter_sampling_gb300 import build
+    build.build()
+    from drafter_sampling_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vt_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ["vt_calibrate_topk", "vt_trim_head", "vt_draft_logits", "vt_draft_step",
+                 "vt_verify"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_cover_header():
+    from drafter_sampling_gb300 import _lib
+    assert set(_declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.vt_abi_version() >= 100
+    for code in [0, -1, -2, -3, -4, -5, 12345]:
+        assert isinstance(lib.vt_status_string(code), bytes)
+
+
+def test_workspace_queries(lib):
+    assert lib.vt_verify_workspace_bytes(16, 6, 128256, 32768) > 0
+    assert lib.vt_verify_workspace_bytes(0, 6, 10, 10) == 0
+    assert lib.vt_draft_workspace_bytes(16, 2048, 32768) > 0
+    assert lib.vt_calibrate_topk_workspace_bytes(1000, 128256, 32768) > 0
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    # null pointers and bad sizes are rejected before any CUDA call
+    st = lib.vt_verify(None, 0, 1, 1, 10, None, None, 5, None, None, None, 1.0,
+                       None, None, None, None, None, 0, None)
+    assert st == _lib.VT_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(256)
+    st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 5, fake, fake, fake, -1.0,
+                       fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # temperature <= 0
+    st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 11, fake, fake, fake, 1.0,
+                       fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # K > V
+    st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 5, fake, fake, fake, 1.0,
+                       fake, fake, None, fake, None, 0, None)
+    assert st == _lib.VT_ERR_WORKSPACE            # no workspace
+    st = lib.vt_verify(fake, 7, 1, 1, 10, fake, fake, 5, fake, fake, fake, 1.0,
+                       fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # unknown dtype
