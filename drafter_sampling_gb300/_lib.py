@@ -17,6 +17,8 @@ VT_ERR_UNSUPPORTED = -2
 VT_ERR_CUDA = -3
 VT_ERR_BAD_INPUT = -4
 VT_ERR_WORKSPACE = -5
+VT_ERR_SCRATCH_LIMIT = -6
+VT_VERIFY_NOALLOC_SCRATCH_BYTES = 2 << 20
 
 VT_F32 = 0
 VT_BF16 = 1
@@ -47,6 +49,8 @@ SIGNATURES = {
     "vt_verify_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "vt_verify": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32, _p,
                             _p, _p, _p, _p, _sz, _p]),
+    "vt_verify_noalloc": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32,
+                                    _p, _p, _p, _p, _p]),
 }
 
 

@@ -9,6 +9,7 @@ extern "C" const char* vt_status_string(int status) {
     case VT_ERR_CUDA: return "CUDA error";
     case VT_ERR_BAD_INPUT: return "bad input data";
     case VT_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case VT_ERR_SCRATCH_LIMIT: return "problem exceeds the library's static scratch";
     default: return "unknown status";
   }
 }

@@ -23,6 +23,7 @@
 // running sums the selection compares are bit-identical in both places.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "vt_common.cuh"
 
@@ -572,4 +573,64 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
   }
   VT_RETURN_IF_LAUNCH_FAILED();
   return VT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// vt_verify_noalloc: the same verification with its scratch in a static
+// device array instead of a caller-provided workspace, for callers that have
+// no device allocator to call (a plug-in inside a runtime that owns all
+// device memory, allocator-free C code, a loop that must not risk
+// cudaMalloc's device-wide synchronisation).  All calls on a device share the
+// array; overlapping calls race on it.
+namespace vt {
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+
+// 2 MiB of scratch per device, resident for the life of the process.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[VT_VERIFY_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device.  Host code only
+// holds a stand-in for the symbol, so the address is looked up once per
+// device (with that device current) and cached.
+int noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[kNoallocMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VT_ERR_CUDA;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return VT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return VT_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return VT_OK;
+}
+
+}  // namespace
+}  // namespace vt
+
+extern "C" int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype, int32_t B,
+                                 int32_t gamma, int32_t V, const float* q,
+                                 const int32_t* inv_map, int32_t K, const int32_t* draft_tokens,
+                                 const float* u_accept, const float* u_resample,
+                                 float temperature, int32_t* out_tokens,
+                                 int32_t* out_num_accepted, float* out_accept_prob,
+                                 int32_t* dev_status, void* stream) {
+  using namespace vt;
+  if (B < 1 || gamma < 1 || gamma > kMaxGamma) return VT_ERR_INVALID_ARG;
+  const size_t need = vt_verify_workspace_bytes(B, gamma, V, K);
+  if (need > VT_VERIFY_NOALLOC_SCRATCH_BYTES) return VT_ERR_SCRATCH_LIMIT;
+  if (!target_logits || !q || !inv_map || !draft_tokens || !u_accept || !u_resample ||
+      !out_tokens || !out_num_accepted || !dev_status)
+    return VT_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch_address(&scratch);
+  if (st != VT_OK) return st;
+  return vt_verify(target_logits, logits_dtype, B, gamma, V, q, inv_map, K, draft_tokens,
+                   u_accept, u_resample, temperature, out_tokens, out_num_accepted,
+                   out_accept_prob, dev_status, scratch, VT_VERIFY_NOALLOC_SCRATCH_BYTES, stream);
 }

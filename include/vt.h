@@ -51,7 +51,9 @@ enum {
   VT_ERR_UNSUPPORTED = -2,  /* valid request this build does not implement */
   VT_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed         */
   VT_ERR_BAD_INPUT = -4,    /* reserved for host-detected bad data          */
-  VT_ERR_WORKSPACE = -5     /* workspace missing, too small or misaligned  */
+  VT_ERR_WORKSPACE = -5,    /* workspace missing, too small or misaligned  */
+  VT_ERR_SCRATCH_LIMIT = -6 /* problem needs more scratch than the library's
+                               static array holds (vt_verify_noalloc)      */
 };
 
 /* Element types of target logits. */
@@ -194,6 +196,43 @@ int vt_verify(const void* target_logits, int32_t logits_dtype,
               int32_t* out_tokens, int32_t* out_num_accepted,
               float* out_accept_prob, int32_t* dev_status,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * vt_verify_noalloc - vt_verify for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point: it changes
+ * nothing in what is computed, only where the scratch lives.
+ *
+ * Some callers have no way to hand the library a workspace: an extension
+ * loaded into a host runtime that owns all device memory and gives its
+ * plug-ins no allocator, C code without a device allocator of its own, or a
+ * latency-critical loop that must not call cudaMalloc (which can
+ * synchronise the whole device).  This variant takes exactly the inputs and
+ * outputs of vt_verify, minus the workspace.  Its scratch is a file-scope
+ * static device array of VT_VERIFY_NOALLOC_SCRATCH_BYTES (2 MiB) inside
+ * libvt, which every GPU that loads the library holds until the process
+ * exits.
+ *  - Limit: a problem whose vt_verify_workspace_bytes(B, gamma, V, K) is
+ *    larger than VT_VERIFY_NOALLOC_SCRATCH_BYTES is rejected with
+ *    VT_ERR_SCRATCH_LIMIT before any device work (about 3800 rows
+ *    B*(gamma+1) fit, e.g. B=256 with gamma=8).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current, and returns
+ *    VT_ERR_CUDA if the lookup fails.  Make that first call before any
+ *    stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps what
+ *    the last call left in it; the kernels clear what must start at zero.
+ *    Calls that can overlap on the GPU (e.g. on two streams with no ordering
+ *    between them) race on the array and give undefined results: order them.
+ *  - The call performs no cudaMalloc, cudaFree or other allocation.
+ * ---------------------------------------------------------------------- */
+#define VT_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)2 << 20)
+int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype,
+                      int32_t B, int32_t gamma, int32_t V,
+                      const float* q, const int32_t* inv_map, int32_t K,
+                      const int32_t* draft_tokens, const float* u_accept,
+                      const float* u_resample, float temperature,
+                      int32_t* out_tokens, int32_t* out_num_accepted,
+                      float* out_accept_prob, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }
