@@ -13,7 +13,8 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
-                   VT_DEV_DUPLICATE_ID, VT_DEV_NONFINITE, VT_DEV_ZERO_RESIDUAL, VT_F32,
+                   VT_DEV_DUPLICATE_ID, VT_DEV_NONFINITE, VT_DEV_TIMEOUT,
+                   VT_DEV_ZERO_RESIDUAL, VT_F32,
                    VtError)
 
 __all__ = ["vt_calibrate_topk", "vt_trim_head", "vt_draft_logits", "vt_draft_step",

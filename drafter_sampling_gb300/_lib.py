@@ -28,6 +28,7 @@ VT_DEV_DUPLICATE_ID = 2
 VT_DEV_BAD_DRAFT = 4
 VT_DEV_NONFINITE = 8
 VT_DEV_ZERO_RESIDUAL = 16
+VT_DEV_TIMEOUT = 32
 
 _p = C.c_void_p
 _i32 = C.c_int32

@@ -1,0 +1,522 @@
+// Drafting through the VocabTrim head on sm_103a.
+//
+// Operation ("VocabTrim: Vocabulary Pruning for Efficient Speculative
+// Decoding in LLMs", Algorithm 2, drafting; temperature as required by the
+// "Speculative decoding" glossary, "Distributional exactness has
+// conditions"):
+//   z[b, j] = (hidden[b] . W_trim[j]) / T     over the K trimmed ids only
+//   q[b, :] = softmax(z[b, :]);  token[b] = trim_ids[j*], j* = strict inverse
+//   CDF of q[b] at u_b in ascending j (ascending target id).
+//
+// Kernels:
+//  1. draft_gemv: streams W_trim once from HBM with 16-byte loads, four lanes
+//     per row (64 contiguous bytes per row per step), the hidden tile in
+//     shared memory (broadcast reads), fp32 FMA accumulation.  Its epilogue
+//     stores z (scaled to base 2 for the softmax) and folds each CTA's rows
+//     into per-row-of-batch online-softmax partials (max, sum 2^(z - max)).
+//  2. draft_finalize grid (B, C): merges the partials, writes q = 2^(z-m)/S
+//     in place, and sums each chunk with a fixed-order tile scan; the last CTA
+//     of row b (atomic ticket, no waiting) finds the chunk where the running
+//     sum passes u_b * sum(q) and rescans it with the same tile scan.
+#include <algorithm>
+#include <cmath>
+
+#include "vt_common.cuh"
+
+namespace vt {
+namespace {
+
+constexpr int kGemvNT = 256;        // 8 warps
+constexpr int kRowsPerWarp = 8;     // 4 lanes per row
+constexpr int kMaxGemvCtas = 1024;
+constexpr int kMaxFinChunks = 64;
+constexpr int kFinNT = 256;
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+
+// out[b, j] = out_scale * sum_h hidden[b, h] * W[j, h] for one tile of BT rows
+// of the batch at a time.  part (optional) receives, per CTA and batch row,
+// the online-softmax partial of the values written.
+template <int BT, int UNROLL>
+__global__ void __launch_bounds__(kGemvNT)
+draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
+                  const uint16_t* __restrict__ W, int K, float out_scale,
+                  float* __restrict__ out, int64_t ldo, float2* __restrict__ part,
+                  int* __restrict__ zero_ints, int nzero, int* __restrict__ status_to_zero,
+                  int vec_ok) {
+  extern __shared__ __align__(16) uint16_t sh_h[];  // [BT][H]
+  __shared__ MS sred[kGemvNT / 32][BT];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane & 3;         // which 16-byte slice of a 64-byte step
+  const int rlane = lane >> 2;      // row within the warp's group of 8
+
+  if (blockIdx.x == 0) {
+    // tickets and status word of the finalize kernel, which starts only
+    // after this grid has completed (same stream)
+    for (int i = tid; i < nzero; i += kGemvNT) zero_ints[i] = 0;
+    if (tid == 0 && status_to_zero != nullptr) *status_to_zero = 0;
+  }
+
+  for (int b0 = 0; b0 < B; b0 += BT) {
+    const int bt = min(BT, B - b0);
+    __syncthreads();
+    // stage hidden rows b0..b0+bt (zero rows past bt)
+    if (vec_ok) {
+      const int hv = H / 8;
+      for (int i = tid; i < BT * hv; i += kGemvNT) {
+        const int b = i / hv, c = i - b * hv;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (b < bt) v = __ldg(reinterpret_cast<const uint4*>(hidden + (int64_t)(b0 + b) * H) + c);
+        reinterpret_cast<uint4*>(sh_h + (int64_t)b * H)[c] = v;
+      }
+    } else {
+      for (int i = tid; i < BT * H; i += kGemvNT) {
+        const int b = i / H, c = i - b * H;
+        sh_h[i] = (b < bt) ? __ldg(hidden + (int64_t)(b0 + b) * H + c) : (uint16_t)0;
+      }
+    }
+    __syncthreads();
+
+    float m[BT], s[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) { m[b] = kNegBig; s[b] = 0.f; }
+
+    const int groups = (K + kRowsPerWarp - 1) / kRowsPerWarp;
+    for (int g = blockIdx.x * (kGemvNT / 32) + warp; g < groups; g += gridDim.x * (kGemvNT / 32)) {
+      const int row = g * kRowsPerWarp + rlane;
+      float acc[BT];
+#pragma unroll
+      for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+      if (row < K) {
+        const uint16_t* wr = W + (int64_t)row * H;
+        if (vec_ok) {
+          // 16-byte slices h = 8*sub + 32*t
+          const int nsteps = H / 32;           // full 64-byte steps
+          int t = 0;
+          for (; t + UNROLL <= nsteps; t += UNROLL) {
+            uint4 wv[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+              wv[u] = __ldg(reinterpret_cast<const uint4*>(wr + 32 * (t + u) + 8 * sub));
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+              float wf[8];
+              unpack_bf16x8(wv[u], wf);
+              const int h = 32 * (t + u) + 8 * sub;
+#pragma unroll
+              for (int b = 0; b < BT; ++b) {
+                float hf[8];
+                unpack_bf16x8(*reinterpret_cast<const uint4*>(sh_h + b * H + h), hf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[b] = fmaf(wf[k], hf[k], acc[b]);
+              }
+            }
+          }
+          for (; t < nsteps; ++t) {
+            const int h = 32 * t + 8 * sub;
+            float wf[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(wr + h)), wf);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+              float hf[8];
+              unpack_bf16x8(*reinterpret_cast<const uint4*>(sh_h + b * H + h), hf);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) acc[b] = fmaf(wf[k], hf[k], acc[b]);
+            }
+          }
+          // remaining H % 32 elements in 16-byte slices
+          const int h = 32 * nsteps + 8 * sub;
+          if (h < H) {
+            float wf[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(wr + h)), wf);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+              float hf[8];
+              unpack_bf16x8(*reinterpret_cast<const uint4*>(sh_h + b * H + h), hf);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) acc[b] = fmaf(wf[k], hf[k], acc[b]);
+            }
+          }
+        } else {
+          for (int h = sub; h < H; h += 4) {
+            const float wf = bf16_bits_to_float(__ldg(wr + h));
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[b] = fmaf(wf, bf16_bits_to_float(sh_h[b * H + h]), acc[b]);
+          }
+        }
+      }
+      // reduce the four lanes of each row
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 1);
+        acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 2);
+      }
+      if (row < K && sub == 0) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          if (b < bt) {
+            const float z = acc[b] * out_scale;
+            out[(int64_t)(b0 + b) * ldo + row] = z;
+            if (z > m[b]) {
+              s[b] *= exp2_approx(m[b] - z);
+              m[b] = z;
+            }
+            s[b] += exp2_approx(z - m[b]);
+          }
+        }
+      }
+    }
+    if (part != nullptr) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        MS v = warp_ms_reduce(MS{m[b], s[b]});
+        if (lane == 0) sred[warp][b] = v;
+      }
+      __syncthreads();
+      if (tid < bt) {
+        MS r = sred[0][tid];
+#pragma unroll
+        for (int w = 1; w < kGemvNT / 32; ++w) r = ms_combine(r, sred[w][tid]);
+        part[(int64_t)blockIdx.x * B + b0 + tid] = make_float2(r.m, r.s);
+      }
+    }
+  }
+}
+
+struct FinArgs {
+  float* q;          // in: z scaled to base 2; out: probabilities
+  int64_t ldq;
+  int B, K;
+  const float2* part;
+  int G;
+  const float* u;
+  const int* trim_ids;
+  int* tokens;
+  float* zpart;
+  int* lpart;
+  int nchunk;
+  int chunk_len;
+  int* counters;
+  int* dev_status;
+  int vec_ok;
+};
+
+// four consecutive values at j (multiple of 4); zeros past j1
+__device__ __forceinline__ void load4f(const float* p, int64_t j, int64_t j1, bool vec, float* x,
+                                       bool l2) {
+  if (vec && j + 3 < j1) {
+    float4 v = l2 ? __ldcg(reinterpret_cast<const float4*>(p + j))
+                  : *reinterpret_cast<const float4*>(p + j);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = (j + e < j1) ? (l2 ? __ldcg(p + j + e) : p[j + e]) : 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
+  __shared__ MS mred[kFinNT / 32];
+  __shared__ float sred[kFinNT / 32];
+  __shared__ int ired[kFinNT / 32];
+  __shared__ int s_last, s_cstar, s_pick;
+  __shared__ float s_target;
+  const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+  float* qrow = a.q + (int64_t)b * a.ldq;
+  const bool vec = a.vec_ok != 0;
+
+  // global (max, sum) of row b from the GEMV partials
+  MS v{kNegBig, 0.f};
+  for (int g = tid; g < a.G; g += kFinNT) {
+    float2 t = a.part[(int64_t)g * a.B + b];
+    v = ms_combine(v, MS{t.x, t.y});
+  }
+  v = block_ms_reduce<kFinNT>(v, mred);
+  if (!(v.s > 0.f && isfinite(v.s) && isfinite(v.m))) {
+    if (c == 0 && tid == 0) {
+      a.tokens[b] = -1;
+      atomicOr(a.dev_status, VT_DEV_NONFINITE);
+    }
+    return;
+  }
+  const float m = v.m, invS = 1.f / v.s;
+
+  // normalise this chunk in place and sum it with the fixed-order tile scan
+  const int64_t j0 = (int64_t)c * a.chunk_len;
+  const int64_t j1 = min((int64_t)a.K, j0 + (int64_t)a.chunk_len);
+  float run = 0.f;
+  int lp = -1;
+  for (int64_t base = j0; base < j1; base += (int64_t)kFinNT * 4) {
+    const int64_t j = base + 4 * (int64_t)tid;
+    float x[4];
+    load4f(qrow, j, j1, vec, x, false);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = (j + e < j1) ? exp2_approx(x[e] - m) * invS : 0.f;
+    if (vec && j + 3 < j1) {
+      *reinterpret_cast<float4*>(qrow + j) = make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j + e < j1) qrow[j + e] = x[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (x[e] > 0.f) lp = (int)(j + e);
+    const float t4 = ((x[0] + x[1]) + x[2]) + x[3];
+    float excl, tot;
+    block_scan_incl<kFinNT>(t4, sred, excl, tot);
+    run += tot;
+  }
+  lp = block_max_int<kFinNT>(lp, ired);
+  if (tid == 0) {
+    a.zpart[(int64_t)b * a.nchunk + c] = run;
+    a.lpart[(int64_t)b * a.nchunk + c] = lp;
+    __threadfence();
+    s_last = (atomicAdd(a.counters + b, 1) == a.nchunk - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  if (tid == 0) {
+    const float* zp = a.zpart + (int64_t)b * a.nchunk;
+    float total = 0.f;
+    for (int k = 0; k < a.nchunk; ++k) total += __ldcg(zp + k);
+    const float target = a.u[b] * total;
+    float pre = 0.f;
+    int cstar = -1;
+    for (int k = 0; k < a.nchunk; ++k) {
+      const float zk = __ldcg(zp + k);
+      if (pre + zk > target) { cstar = k; break; }
+      pre += zk;
+    }
+    int glast = -1;
+    for (int k = 0; k < a.nchunk; ++k) glast = max(glast, __ldcg(a.lpart + (int64_t)b * a.nchunk + k));
+    s_cstar = cstar;
+    s_target = target - pre;
+    s_pick = glast;
+  }
+  __syncthreads();
+  int pick = s_pick;
+  if (s_cstar >= 0) {
+    const int64_t c0 = (int64_t)s_cstar * a.chunk_len;
+    const int64_t c1 = min((int64_t)a.K, c0 + (int64_t)a.chunk_len);
+    const float target = s_target;
+    float run2 = 0.f;
+    int lp2 = -1;
+    __syncthreads();
+    if (tid == 0) s_pick = -1;
+    __syncthreads();
+    for (int64_t base = c0; base < c1; base += (int64_t)kFinNT * 4) {
+      const int64_t j = base + 4 * (int64_t)tid;
+      float x[4];
+      load4f(qrow, j, c1, vec, x, true);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (x[e] > 0.f) lp2 = (int)(j + e);
+      const float t4 = ((x[0] + x[1]) + x[2]) + x[3];
+      float excl, tot;
+      const float incl = block_scan_incl<kFinNT>(t4, sred, excl, tot);
+      const bool hit = (run2 + incl > target);
+      const int first = block_min_int<kFinNT>(hit ? tid : kFinNT, ired);
+      if (first < kFinNT) {
+        if (tid == first) {
+          float acc = run2 + excl;
+          int pk = -1, lastp = -1;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (x[e] > 0.f) lastp = (int)(j + e);
+            acc += x[e];
+            if (pk < 0 && acc > target) pk = (int)(j + e);
+          }
+          s_pick = (pk >= 0) ? pk : lastp;
+        }
+        __syncthreads();
+        break;
+      }
+      run2 += tot;
+    }
+    lp2 = block_max_int<kFinNT>(lp2, ired);
+    pick = (s_pick >= 0) ? s_pick : (lp2 >= 0 ? lp2 : pick);
+  }
+  if (tid == 0) {
+    a.tokens[b] = (pick >= 0) ? a.trim_ids[pick] : -1;
+    a.counters[b] = 0;
+  }
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+struct DraftWs {
+  float2* part;
+  float* zpart;
+  int* lpart;
+  int* counters;
+  size_t bytes;
+};
+
+DraftWs carve_draft(void* base, int B) {
+  DraftWs w;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    size_t o = off;
+    off = align_up(off + n, 256);
+    return o;
+  };
+  size_t o_part = take((size_t)kMaxGemvCtas * B * sizeof(float2));
+  size_t o_z = take((size_t)B * kMaxFinChunks * sizeof(float));
+  size_t o_l = take((size_t)B * kMaxFinChunks * sizeof(int));
+  size_t o_c = take((size_t)B * sizeof(int));
+  char* p = static_cast<char*>(base);
+  w.part = reinterpret_cast<float2*>(p + o_part);
+  w.zpart = reinterpret_cast<float*>(p + o_z);
+  w.lpart = reinterpret_cast<int*>(p + o_l);
+  w.counters = reinterpret_cast<int*>(p + o_c);
+  w.bytes = off;
+  return w;
+}
+
+int gemv_bt(int B) {
+  if (B >= 16) return 16;
+  if (B >= 8) return 8;
+  if (B >= 4) return 4;
+  if (B >= 2) return 2;
+  return 1;
+}
+
+template <int BT>
+cudaError_t launch_gemv_bt(int grid, cudaStream_t s, const uint16_t* hidden, int B, int H,
+                           const uint16_t* W, int K, float out_scale, float* out, int64_t ldo,
+                           float2* part, int* zero_ints, int nzero, int* status_to_zero,
+                           int vec_ok) {
+  const size_t smem = (size_t)BT * H * sizeof(uint16_t);
+  auto kern = draft_gemv_kernel<BT, 4>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kGemvNT, smem, s>>>(hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
+                                   status_to_zero, vec_ok);
+  return cudaGetLastError();
+}
+
+int launch_gemv(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
+                float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints,
+                int nzero, int* status_to_zero, int* grid_out) {
+  const int vec_ok = (H % 8 == 0) && ((reinterpret_cast<uintptr_t>(hidden) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
+  int bt = gemv_bt(B);
+  // the hidden tile must fit in shared memory
+  while (bt > 1 && (size_t)bt * H * 2 > 160 * 1024) bt >>= 1;
+  if ((size_t)bt * H * 2 > 200 * 1024) return VT_ERR_UNSUPPORTED;
+  const int rows_per_cta = (kGemvNT / 32) * kRowsPerWarp;
+  int grid = (K + rows_per_cta - 1) / rows_per_cta;
+  grid = std::max(1, std::min(grid, std::min(kMaxGemvCtas, 2 * num_sms())));
+  *grid_out = grid;
+  cudaError_t e;
+  switch (bt) {
+    case 16: e = launch_gemv_bt<16>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+    case 8: e = launch_gemv_bt<8>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+    case 4: e = launch_gemv_bt<4>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+    case 2: e = launch_gemv_bt<2>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+    default: e = launch_gemv_bt<1>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+  }
+  return e == cudaSuccess ? VT_OK : VT_ERR_CUDA;
+}
+
+int check_draft_args(const uint16_t* hidden, int B, int H, const uint16_t* W_trim, int K,
+                     float T) {
+  if (!hidden || !W_trim) return VT_ERR_INVALID_ARG;
+  if (B < 1 || B > 4096 || H < 1 || H > 65536 || K < 1) return VT_ERR_INVALID_ARG;
+  if (!(T > 0.f) || !std::isfinite(T)) return VT_ERR_INVALID_ARG;
+  return VT_OK;
+}
+
+}  // namespace
+}  // namespace vt
+
+extern "C" size_t vt_draft_workspace_bytes(int32_t B, int32_t H, int32_t K) {
+  (void)H;
+  (void)K;
+  if (B < 1) return 0;
+  return vt::carve_draft(nullptr, B).bytes;
+}
+
+extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
+                               const uint16_t* W_trim, int32_t K, float temperature,
+                               float* logits, int64_t ld_logits, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  using namespace vt;
+  int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
+  if (st != VT_OK) return st;
+  if (!logits || ld_logits < K) return VT_ERR_INVALID_ARG;
+  (void)workspace;
+  (void)workspace_bytes;
+  int grid = 0;
+  return launch_gemv(static_cast<cudaStream_t>(stream), hidden, B, H, W_trim, K,
+                     1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, nullptr, &grid);
+}
+
+extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
+                             const uint16_t* W_trim, const int32_t* trim_ids, int32_t K,
+                             const float* uniforms, float temperature, float* q, int64_t ldq,
+                             int32_t* tokens, int32_t* dev_status, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  using namespace vt;
+  int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
+  if (st != VT_OK) return st;
+  if (!trim_ids || !uniforms || !q || ldq < K || !tokens || !dev_status) return VT_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
+  DraftWs ws = carve_draft(workspace, B);
+  if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  int grid = 0;
+  st = launch_gemv(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part,
+                   ws.counters, B, dev_status, &grid);
+  if (st != VT_OK) return st;
+
+  FinArgs fa;
+  fa.q = q;
+  fa.ldq = ldq;
+  fa.B = B;
+  fa.K = K;
+  fa.part = ws.part;
+  fa.G = grid;
+  fa.u = uniforms;
+  fa.trim_ids = trim_ids;
+  fa.tokens = tokens;
+  fa.zpart = ws.zpart;
+  fa.lpart = ws.lpart;
+  int nchunk = (num_sms() * 4 + B - 1) / B;
+  nchunk = std::max(1, std::min(nchunk, kMaxFinChunks));
+  nchunk = std::min(nchunk, std::max(1, K / 1024));
+  int len = (K + nchunk - 1) / nchunk;
+  len = (len + 3) / 4 * 4;
+  nchunk = (K + len - 1) / len;
+  fa.nchunk = nchunk;
+  fa.chunk_len = len;
+  fa.counters = ws.counters;
+  fa.dev_status = dev_status;
+  fa.vec_ok = ((reinterpret_cast<uintptr_t>(q) & 15) == 0) && (ldq % 4 == 0);
+  dim3 g2((unsigned)B, (unsigned)nchunk);
+  draft_finalize_kernel<<<g2, kFinNT, 0, s>>>(fa);
+  VT_RETURN_IF_LAUNCH_FAILED();
+  return VT_OK;
+}

@@ -66,8 +66,10 @@ enum {
   VT_DEV_BAD_DRAFT = 4,      /* drafted token out of range, not trimmed, or
                                 q(x) <= 0 at a drafted token                    */
   VT_DEV_NONFINITE = 8,      /* NaN/Inf reached a softmax normaliser           */
-  VT_DEV_ZERO_RESIDUAL = 16  /* informational: residual mass was zero at a
+  VT_DEV_ZERO_RESIDUAL = 16, /* informational: residual mass was zero at a
                                 rejection; that draw used p instead            */
+  VT_DEV_TIMEOUT = 32        /* an internal wait between thread blocks gave up
+                                (bounded spin); the affected outputs are unset */
 };
 
 /* Human-readable text for a return code. Never NULL. */
@@ -184,8 +186,8 @@ int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
  *                                 position (0..min(n_b, gamma-1)); NaN at
  *                                 positions after the first rejection
  *  dev_status int32 [1]           out: VT_DEV_BAD_DRAFT, VT_DEV_NONFINITE,
- *                                 VT_DEV_ZERO_RESIDUAL
- * 1 <= gamma <= 64, 1 <= B, 1 <= K <= V.
+ *                                 VT_DEV_ZERO_RESIDUAL, VT_DEV_TIMEOUT
+ * 1 <= gamma <= 64, 1 <= B, 1 <= K <= V <= 2^22.
  * ---------------------------------------------------------------------- */
 size_t vt_verify_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t K);
 int vt_verify(const void* target_logits, int32_t logits_dtype,

@@ -42,9 +42,24 @@ def assert_logits_close(gpu, ref, what="logits"):
                              f"gpu={gpu[tuple(i)]!r} ref={ref[tuple(i)]!r}")
 
 
-def compare_verify(tokens, n_acc, accept_prob, ref, boundary=BOUNDARY):
+def draw_is_valid(weights, u, index, tol=BOUNDARY):
+    """For a draw excluded as a boundary case: the chosen bin must lie within
+    ``tol`` of the uniform in the oracle's fp64 CDF, and have positive weight."""
+    w = np.asarray(weights, dtype=np.float64)
+    if not (0 <= index < w.size) or not w[index] > 0:
+        return False
+    cdf = np.cumsum(w) / w.sum()
+    lo = cdf[index - 1] if index > 0 else 0.0
+    hi = cdf[index]
+    return lo - tol <= float(u) < hi + tol
+
+
+def compare_verify(tokens, n_acc, accept_prob, ref, boundary=BOUNDARY, draw_weights=None):
     """Compare vt_verify outputs with oracle.verify's VerifyResult.
 
+    ``draw_weights(b, n)`` (optional) returns the oracle's fp64 weights of the
+    final draw of sequence b; with it, boundary draws are checked for
+    validity instead of skipped.
     Returns dict(compared=..., excluded_seq=..., excluded_draw=...).
     """
     tokens = np.asarray(tokens)
@@ -68,6 +83,10 @@ def compare_verify(tokens, n_acc, accept_prob, ref, boundary=BOUNDARY):
             assert np.all(np.isnan(np.asarray(accept_prob)[b, tested:])), f"seq {b}: NaN tail"
         if ref.draw_margin[b] <= boundary:
             stats["excluded_draw"] += 1
+            if draw_weights is not None:
+                w, u = draw_weights(b, n_ref)
+                assert draw_is_valid(w, u, int(tokens[b, n_ref])), (
+                    f"seq {b}: boundary draw {int(tokens[b, n_ref])} not within tolerance")
         else:
             assert int(tokens[b, n_ref]) == int(ref.tokens[b, n_ref]), (
                 f"seq {b}: drawn token {int(tokens[b, n_ref])} vs oracle {int(ref.tokens[b, n_ref])}"

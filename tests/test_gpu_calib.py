@@ -1,0 +1,148 @@
+"""vt_calibrate_topk / vt_trim_head (CUDA, through the C ABI) against the
+oracle: bit-exact counts, ranked ids, trimmed rows and maps."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import drafter_sampling_gb300 as m
+    from drafter_sampling_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _calib(vt, ids, V, K):
+    c, t, st = vt.vt_calibrate_topk(_dev(ids), V, K)
+    torch.cuda.synchronize()
+    return c.cpu().numpy().view(np.uint32), t.cpu().numpy(), int(st.item())
+
+
+@pytest.mark.parametrize("V,N,K,s", [
+    (3001, 100_003, 257, 1.1),
+    (3001, 100_003, 3001, 1.1),     # K = V: a full ranking
+    (1000, 50_000, 1, 0.5),         # K = 1
+    (70_000, 1_000_001, 5000, 1.1),
+    (17, 9, 5, 1.1),                # many zero counts (ties at 0)
+])
+def test_histogram_and_topk_bit_exact(vt, V, N, K, s):
+    ids = synthetic.zipf_ids(N, V, s=s, seed=V + N)
+    c, t, st = _calib(vt, ids, V, K)
+    assert st == 0
+    ref_c = oracle.token_histogram(ids, V)
+    assert np.array_equal(c.astype(np.int64), ref_c)
+    assert np.array_equal(t, oracle.top_k(ref_c, K))
+
+
+def test_heavy_ties(vt):
+    # 600 ids, counts drawn from {0,1,2,3}: ties everywhere, lower id wins
+    g = synthetic.rng(90, 0)
+    V = 600
+    target = g.integers(0, 4, V)
+    ids = np.repeat(np.arange(V, dtype=np.int32), target)
+    ids = ids[g.permutation(ids.size)]
+    for K in [1, 100, 599, 600]:
+        c, t, st = _calib(vt, ids, V, K)
+        assert np.array_equal(c.astype(np.int64), target)
+        assert np.array_equal(t, oracle.top_k(target, K))
+
+
+def test_empty_stream(vt):
+    c, t, st = _calib(vt, np.zeros(0, np.int32), 50, 7)
+    assert st == 0 and not c.any()
+    assert list(t) == list(range(7))
+
+
+def test_out_of_range_ids_flagged_and_skipped(vt):
+    ids = np.array([1, 2, -1, 2, 50, 3, 2], np.int32)
+    c, t, st = _calib(vt, ids, 50, 3)
+    assert st & vt.VT_DEV_BAD_ID
+    good = ids[(ids >= 0) & (ids < 50)]
+    assert np.array_equal(c.astype(np.int64), np.bincount(good, minlength=50))
+    assert list(t) == [2, 1, 3]
+
+
+def test_unaligned_id_stream(vt):
+    # a view starting one element in: scalar loads
+    ids = synthetic.zipf_ids(10_007, 999, seed=5)
+    full = _dev(ids)
+    view = full[1:]
+    c, t, st = vt.vt_calibrate_topk(view, 999, 50)
+    torch.cuda.synchronize()
+    ref_c = oracle.token_histogram(ids[1:], 999)
+    assert np.array_equal(c.cpu().numpy().view(np.uint32).astype(np.int64), ref_c)
+    assert np.array_equal(t.cpu().numpy(), oracle.top_k(ref_c, 50))
+
+
+def test_calibration_full_size(vt):
+    # 50M Zipf(1.1) ids over V=128256; K in {8192, 16384, 32768, 65536}
+    V, N = 128256, 50_000_000
+    ids = synthetic.zipf_ids(N, V, s=1.1, seed=synthetic.SEED_CALIB)
+    ref_c = oracle.token_histogram(ids, V)
+    d_ids = _dev(ids)
+    for K in [8192, 16384, 32768, 65536]:
+        c, t, st = vt.vt_calibrate_topk(d_ids, V, K)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert np.array_equal(c.cpu().numpy().view(np.uint32).astype(np.int64), ref_c)
+        assert np.array_equal(t.cpu().numpy(), oracle.top_k(ref_c, K))
+
+
+@pytest.mark.parametrize("V,H,K", [(500, 24, 77), (1000, 13, 999), (64, 8, 64), (300, 3072, 1)])
+def test_trim_head_bit_exact(vt, V, H, K):
+    g = synthetic.rng(V + H + K, 0)
+    W = g.integers(0, 65535, (V, H)).astype(np.uint16)
+    topk = g.permutation(V)[:K].astype(np.int32)
+    Wt, ti, im, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(topk))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rW, rti, rim = oracle.trim_head(W, topk)
+    assert np.array_equal(Wt.cpu().numpy().view(np.uint16), rW)
+    assert np.array_equal(ti.cpu().numpy(), rti)
+    assert np.array_equal(im.cpu().numpy(), rim)
+
+
+def test_trim_head_full_size(vt):
+    # W [128256, 3072] bf16 N(0,0.02); trim to the calibrated top-K
+    V, H = 128256, 3072
+    W = synthetic.head_weights(V, H, seed=synthetic.SEED_CALIB)
+    ids = synthetic.zipf_ids(5_000_000, V, s=1.1, seed=synthetic.SEED_CALIB)
+    d_W = _dev(W.view(np.int16))
+    _, topk, _ = vt.vt_calibrate_topk(_dev(ids), V, 65536)
+    topk_h = topk.cpu().numpy()
+    for K in [8192, 16384, 32768, 65536]:
+        Wt, ti, im, st = vt.vt_trim_head(d_W, topk[:K].contiguous())
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        rW, rti, rim = oracle.trim_head(W, topk_h[:K])
+        assert np.array_equal(ti.cpu().numpy(), rti)
+        assert np.array_equal(im.cpu().numpy(), rim)
+        if K == 32768:
+            assert np.array_equal(Wt.cpu().numpy().view(np.uint16), rW)
+        else:
+            rows = synthetic.rng(K, 1).integers(0, K, 512)
+            assert np.array_equal(Wt[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16),
+                                  rW[rows])
+
+
+def test_trim_head_flags_duplicates_and_range(vt):
+    W = np.arange(40, dtype=np.uint16).reshape(10, 4)
+    _, _, _, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array([1, 3, 3], np.int32)))
+    torch.cuda.synchronize()
+    assert int(st.item()) & vt.VT_DEV_DUPLICATE_ID
+    _, _, _, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array([1, 10], np.int32)))
+    torch.cuda.synchronize()
+    assert int(st.item()) & vt.VT_DEV_BAD_ID

@@ -49,6 +49,22 @@ def _oracle(d, T=1.0):
                          d["u_resample"], T, logits_dtype=d["logits_dtype"])
 
 
+def _weights(d, T=1.0):
+    """Oracle fp64 weights of the final draw of sequence b at position n."""
+    def f(b, n):
+        l = d["logits"][b, n]
+        l = oracle.bf16_to_f64(l) if d["logits_dtype"] == "bf16" else l
+        p = oracle.softmax(l, T)
+        gamma = d["q"].shape[1]
+        if n == gamma:
+            return p, d["u_resample"][b, n]
+        qf = np.zeros_like(p)
+        present = d["inv_map"] >= 0
+        qf[present] = d["q"][b, n, d["inv_map"][present]]
+        return oracle.residual_weights(p, qf), d["u_resample"][b, n]
+    return f
+
+
 def test_two_token_example(vt):
     with open(os.path.join(GOLDEN, "two_token.json")) as f:
         g = json.load(f)
@@ -91,7 +107,7 @@ def test_parity_small(vt, B, gamma, V, K, dt, T, noise):
         toks, n, acc, st = _run(vt, d, T)
         assert st == 0
         ref = _oracle(d, T)
-        s = compare_verify(toks, n, acc, ref)
+        s = compare_verify(toks, n, acc, ref, draw_weights=_weights(d, T))
         for k in totals:
             totals[k] += s[k]
     assert totals["compared"] >= 3 * B - 1, totals
@@ -104,7 +120,7 @@ def test_parity_batched_verify_full_size(vt):
         toks, n, acc, st = _run(vt, d)
         assert st == 0
         ref = _oracle(d)
-        s = compare_verify(toks, n, acc, ref)
+        s = compare_verify(toks, n, acc, ref, draw_weights=_weights(d))
         assert s["compared"] >= 15, s
 
 
@@ -115,7 +131,7 @@ def test_parity_large_batch_bf16_full_size(vt):
     toks, n, acc, st = _run(vt, d, 0.7)
     assert st == 0
     ref = _oracle(d, 0.7)
-    s = compare_verify(toks, n, acc, ref)
+    s = compare_verify(toks, n, acc, ref, draw_weights=_weights(d, 0.7))
     assert s["compared"] >= 250, s
 
 
