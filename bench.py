@@ -2,9 +2,17 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
-Prints ONE JSON line (rank 0).  See the measurement section of the design
-notes for the definition of a step, the algorithmic byte counts and the
-roofline denominators.
+One step is one pass of every hot-path row over one batch of synthetic input,
+at the batched-verify workload's sizes (B=16 sequences, gamma=6, V=128256,
+K=32768, fp32 target logits, head hidden size 2048):
+
+  calibrate   vt_calibrate_topk over 50M Zipf(1.1) token ids -> counts, Top-K
+  trim        vt_trim_head: W [128256, 2048] bf16 -> W_trim [32768, 2048]
+  draft x6    vt_draft_step: hidden [16, 2048] bf16 -> q[:, j, :], tokens[:, j]
+  verify      vt_verify: logits [16, 7, 128256] fp32, q, tokens -> tokens, n
+
+The metric is verified draft positions per second: B*gamma = 96 positions per
+step divided by the step time.  Prints ONE JSON line (rank 0).
 """
 from __future__ import annotations
 
@@ -28,13 +36,16 @@ import synthetic  # noqa: E402
 METRIC = "verified draft positions/sec (B=16, γ=6, V=128256, K=32768) + % of HBM BW"
 UNIT = "positions/s"
 L2_BYTES = 129 * 1000 * 1000
-B, GAMMA, V, K = 16, 6, 128256, 32768
+B, GAMMA, V, K, H = 16, 6, 128256, 32768, 2048
+N_CAL = 50_000_000
+T = 1.0
+ROWS = ["calibrate", "trim", "draft", "verify"]
 
 
+# ---------------------------------------------------------------- helpers
 def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     except Exception:
@@ -42,13 +53,82 @@ def peaks():
 
 
 def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
-# ------------------------------------------------------------------- clocks
+def algorithmic_bytes():
+    """Bytes each call must move at least once (decimal), per call."""
+    return {
+        # ids read, counts written, counts read by the selection, Top-K written
+        "calibrate": N_CAL * 4 + V * 4 + V * 4 + K * 4,
+        # selected rows read and written, ids in/out, inverse map written
+        "trim": 2 * K * H * 2 + K * 4 * 2 + V * 4,
+        # trimmed head read once, hidden read, q written, tokens/uniforms
+        "draft": K * H * 2 + B * H * 2 + B * K * 4 + B * 4 * 2,
+        # logits once, one q row per sequence, inv_map, the drafted ids and
+        # their q, uniforms, outputs
+        "verify": (B * (GAMMA + 1) * V * 4 + B * K * 4 + V * 4 + B * GAMMA * 4 * 3
+                   + B * (GAMMA + 1) * 4 + B * (GAMMA + 1) * 4 + B * 4 + B * GAMMA * 4),
+    }
+
+
+CALLS_PER_STEP = {"calibrate": 1, "trim": 1, "draft": GAMMA, "verify": 1}
+# kernels of this library launched per call (memsets issued by the driver
+# are not counted)
+KERNELS_PER_CALL = {"calibrate": 17, "trim": 4, "draft": 2, "verify": 2}
+
+KERNEL_SOURCES = {
+    "calibrate": ["drafter_sampling_gb300/csrc/vt_calib.cu"],
+    "trim": ["drafter_sampling_gb300/csrc/vt_calib.cu"],
+    "draft": ["drafter_sampling_gb300/csrc/vt_draft.cu"],
+    "verify": ["drafter_sampling_gb300/csrc/vt_verify.cu"],
+}
+
+
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths + ["drafter_sampling_gb300/csrc/vt_common.cuh"]:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(row: str):
+    """DRAM bytes per call from the committed ncu summary, if it was captured
+    on the current source of that call's kernels; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+        e = d[row]
+        if e.get("source_digest") != source_digest(KERNEL_SOURCES[row]):
+            return None
+        return float(e["dram_bytes_per_call"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- inputs
+class HostInputs:
+    """Seeded synthetic inputs of one step (numpy, host)."""
+
+    def __init__(self):
+        perm = synthetic.rank_permutation(V)
+        self.ids = synthetic.zipf_ids(N_CAL, V, s=1.1, seed=synthetic.SEED_CALIB, perm=perm)
+        self.W = synthetic.head_weights(V, H, seed=synthetic.SEED_CALIB)
+        self.hidden = synthetic.hidden_states((GAMMA, B, H), seed=synthetic.SEED_VERIFY)
+        self.u_draft = synthetic.uniforms(synthetic.SEED_VERIFY, 6, (GAMMA, B))
+        vi = synthetic.verify_inputs(B=B, gamma=GAMMA, V=V, K=K, seed=synthetic.SEED_VERIFY)
+        self.logits = vi["logits"]
+        self.u_accept = vi["u_accept"]
+        self.u_resample = vi["u_resample"]
+
+    def step_inputs(self):
+        return dict(ids=self.ids, W=self.W, hidden=self.hidden, u_draft=self.u_draft,
+                    logits=self.logits, u_accept=self.u_accept, u_resample=self.u_resample)
+
+
+# ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
@@ -92,9 +172,8 @@ class ClockSampler:
         rows = []
         for t, line in self.samples:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            rows.append((t, parts))
+            if len(parts) >= 8:
+                rows.append((t, parts))
         inwin = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1] or rows
         if not inwin:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
@@ -117,137 +196,176 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inwin)}
 
 
-# --------------------------------------------------------------- the step
-class VerifyStep:
-    """One pass of the path over one batch: vt_verify on B=16, gamma=6,
-    V=128256, K=32768 fp32 logits."""
+# -------------------------------------------------------------- GPU step
+class GpuStep:
+    """Device buffers, outputs and workspaces of one step."""
 
-    kernels_per_step = 2
-
-    def __init__(self, torch, vt, dev, nsets):
+    def __init__(self, torch, vt, dev, host: HostInputs, nsets: int):
         self.torch, self.vt, self.dev = torch, vt, dev
-        d = synthetic.verify_inputs(B=B, gamma=GAMMA, V=V, K=K, seed=synthetic.SEED_VERIFY)
-        self.host = d
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-        base = dict(logits=t(d["logits"]), q=t(d["q"]), draft=t(d["draft"]),
-                    u_acc=t(d["u_accept"]), u_res=t(d["u_resample"]))
-        self.inv_map = t(d["inv_map"])
-        # distinct buffers so that consecutive steps never hit in L2
-        self.sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
-        self.out_tokens = torch.empty((B, GAMMA + 1), dtype=torch.int32, device=dev)
-        self.out_n = torch.empty(B, dtype=torch.int32, device=dev)
+        self.ids = t(host.ids)
+        self.W = t(host.W.view(np.int16))
+        self.hidden = t(host.hidden.view(np.int16))
+        self.u_draft = t(host.u_draft)
+        base = dict(logits=t(host.logits), u_acc=t(host.u_accept), u_res=t(host.u_resample))
+        self.vsets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+        i32 = torch.int32
+        self.counts = torch.empty(V, dtype=i32, device=dev)
+        self.topk = torch.empty(K, dtype=i32, device=dev)
+        self.W_trim = torch.empty((K, H), dtype=torch.int16, device=dev)
+        self.trim_ids = torch.empty(K, dtype=i32, device=dev)
+        self.inv_map = torch.empty(V, dtype=i32, device=dev)
+        self.q = torch.empty((B, GAMMA, K), dtype=torch.float32, device=dev)
+        self.tokens = torch.empty((B, GAMMA), dtype=i32, device=dev)
+        self.out_tokens = torch.empty((B, GAMMA + 1), dtype=i32, device=dev)
+        self.out_n = torch.empty(B, dtype=i32, device=dev)
         self.out_acc = torch.empty((B, GAMMA), dtype=torch.float32, device=dev)
-        self.status = torch.empty(1, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(vt.workspace_bytes("verify", B=B, gamma=GAMMA, V=V, K=K),
-                              dtype=torch.uint8, device=dev)
-        self.step_input_bytes = sum(v.numel() * v.element_size() for v in base.values())
+        self.status = torch.zeros(4, dtype=i32, device=dev)
+        u8 = torch.uint8
+        self.ws_cal = torch.empty(vt.workspace_bytes("calibrate", n=N_CAL, V=V, K=K), dtype=u8,
+                                  device=dev)
+        self.ws_trim = torch.empty(vt.workspace_bytes("trim", V=V, K=K), dtype=u8, device=dev)
+        self.ws_draft = torch.empty(vt.workspace_bytes("draft", B=B, H=H, K=K), dtype=u8,
+                                    device=dev)
+        self.ws_ver = torch.empty(vt.workspace_bytes("verify", B=B, gamma=GAMMA, V=V, K=K),
+                                  dtype=u8, device=dev)
+        self.nsets = nsets
 
-    @staticmethod
-    def algorithmic_bytes():
-        logits = B * (GAMMA + 1) * V * 4
-        q_rows = B * K * 4                  # one q row per sequence (residual)
-        inv_map = V * 4
-        small = (B * GAMMA * 4 * 3          # drafted ids, their q, u_accept
-                 + B * (GAMMA + 1) * 4      # u_resample
-                 + B * (GAMMA + 1) * 4 + B * 4 + B * GAMMA * 4)   # outputs
-        return logits + q_rows + inv_map + small
-
-    def call(self, s):
+    def run(self, k: int, events=None):
+        """One step; `events` maps row -> list of (start, end) events to record."""
         vt = self.vt
-        vt.vt_verify(s["logits"], s["q"], self.inv_map, s["draft"], s["u_acc"], s["u_res"], 1.0,
+        s = self.vsets[k % self.nsets]
+
+        def mark(row, i):
+            if events is not None:
+                events[row][i].record()
+
+        mark("calibrate", 0)
+        vt.vt_calibrate_topk(self.ids, V, K, counts=self.counts, topk_ids=self.topk,
+                             dev_status=self.status[0:1], workspace=self.ws_cal)
+        mark("calibrate", 1)
+        mark("trim", 0)
+        vt.vt_trim_head(self.W, self.topk, W_trim=self.W_trim, trim_ids=self.trim_ids,
+                        inv_map=self.inv_map, dev_status=self.status[1:2],
+                        workspace=self.ws_trim)
+        mark("trim", 1)
+        for j in range(GAMMA):
+            mark("draft", 2 * j)
+            vt.vt_draft_step(self.hidden[j], self.W_trim, self.trim_ids, self.u_draft[j], T,
+                             q=self.q[:, j, :], tokens=self.tokens[:, j],
+                             dev_status=self.status[2:3], workspace=self.ws_draft)
+            mark("draft", 2 * j + 1)
+        mark("verify", 0)
+        vt.vt_verify(s["logits"], self.q, self.inv_map, self.tokens, s["u_acc"], s["u_res"], T,
                      out_tokens=self.out_tokens, out_num_accepted=self.out_n,
-                     out_accept_prob=self.out_acc, dev_status=self.status, workspace=self.ws)
+                     out_accept_prob=self.out_acc, dev_status=self.status[3:4],
+                     workspace=self.ws_ver)
+        mark("verify", 1)
 
 
-def source_digest(paths):
-    h = hashlib.sha256()
-    for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
-
-
-def traffic_for(kernel_key: str, sources):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel; else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    try:
-        with open(path) as f:
-            d = json.load(f)
-        e = d[kernel_key]
-        if e.get("source_digest") != source_digest(sources):
-            return None
-        return float(e["dram_bytes_per_launch"])
-    except Exception:
-        return None
-
-
-def cpu_baseline_verify(budget_s: float = 12.0):
-    """The oracle, as it stands, on a bounded sample of the same workload:
-    whole sequences of the B=16 batch, one at a time, for about budget_s."""
+# ------------------------------------------------- the oracle on the host
+def oracle_sample(host: HostInputs, k: int):
+    """Time the CPU oracle on sample k of every row; returns per-row seconds
+    scaled to one full step (the sample fraction of each row is stated)."""
     import oracle
-    d = synthetic.verify_inputs(B=B, gamma=GAMMA, V=V, K=K, seed=synthetic.SEED_VERIFY)
-    t0 = time.time()
+    out = {}
+    n_s = N_CAL // 512
+    lo = (k % 512) * n_s
+    t0 = time.perf_counter()
+    counts = oracle.token_histogram(host.ids[lo:lo + n_s], V)
+    t1 = time.perf_counter()
+    topk = oracle.top_k(counts, K)
+    t2 = time.perf_counter()
+    out["calibrate"] = (t1 - t0) * 512 + (t2 - t1)
+    kk = K // 64
+    W_trim, trim_ids, inv_map = oracle.trim_head(host.W, topk[:kk])
+    t3 = time.perf_counter()
+    out["trim"] = (t3 - t2) * 64
+    b = k % B
+    j = k % GAMMA
+    sl = slice(b, b + 1)
+    d = oracle.draft_step(host.hidden[j][sl], W_trim, trim_ids, host.u_draft[j][sl], T)
+    t4 = time.perf_counter()
+    out["draft"] = (t4 - t3) * B * (K / kk) * GAMMA
+    # verify one sequence with a q built over the sample's trimmed set
+    q = np.zeros((1, GAMMA, kk))
+    q[:, :, :] = d["q"][0]
+    draft = np.repeat(d["tokens"][None, :], GAMMA, axis=1)
+    t5 = time.perf_counter()
+    oracle.verify(host.logits[sl], q, inv_map, draft, host.u_accept[sl], host.u_resample[sl], T)
+    t6 = time.perf_counter()
+    out["verify"] = (t6 - t5) * B
+    return out
+
+
+ORACLE_SAMPLE_TEXT = ("per sample: histogram of 1/512 of the 50M ids (x512) + full Top-K; "
+                      "trim of 1/64 of the K rows (x64); one drafter row of one position over "
+                      "the 1/64 trimmed head (x B*gamma*64); one verified sequence (x B); "
+                      "numpy fp64 oracle")
+
+
+def run_oracle_for(seconds: float, host: HostInputs, max_samples=None):
+    t_start = time.time()
     c0 = time.process_time()
-    seqs = 0
-    while time.time() - t0 < budget_s:
-        b = seqs % B
-        sl = slice(b, b + 1)
-        oracle.verify(d["logits"][sl], d["q"][sl], d["inv_map"], d["draft"][sl],
-                      d["u_accept"][sl], d["u_resample"][sl], 1.0)
-        seqs += 1
-    wall = time.time() - t0
+    tot = {r: 0.0 for r in ROWS}
+    n = 0
+    while time.time() - t_start < seconds and (max_samples is None or n < max_samples):
+        s = oracle_sample(host, n)
+        for r in ROWS:
+            tot[r] += s[r]
+        n += 1
+    wall = time.time() - t_start
     cpu = time.process_time() - c0
-    return {"value": seqs * GAMMA / wall, "unit": UNIT, "cores": max(1, round(cpu / wall)),
-            "kind": "oracle",
-            "sample": f"{seqs} whole sequences (gamma={GAMMA}, V={V}) of the B=16 batch, "
-                      f"fp64 numpy, {wall:.1f} s"}
+    per_step = sum(tot.values()) / n
+    return n, per_step, wall, max(1, round(cpu / wall)), {r: tot[r] / n for r in ROWS}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import oracle
-    d = synthetic.verify_inputs(B=B, gamma=GAMMA, V=V, K=K, seed=synthetic.SEED_VERIFY)
-
-    def step(k):
-        b = k % B
-        sl = slice(b, b + 1)
-        oracle.verify(d["logits"][sl], d["q"][sl], d["inv_map"], d["draft"][sl],
-                      d["u_accept"][sl], d["u_resample"][sl], 1.0)
+    host = HostInputs()
     for k in range(args.warmup):
-        step(k)
-    t0 = time.time()
+        oracle_sample(host, k)
+    tot = 0.0
     c0 = time.process_time()
+    t0 = time.time()
     for k in range(args.steps):
-        step(k)
+        tot += sum(oracle_sample(host, k).values())
     wall = time.time() - t0
     cpu = time.process_time() - c0
-    value = args.steps * GAMMA / wall
+    per_step = tot / args.steps
+    value = B * GAMMA / per_step
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "batched verify B=16 gamma=6 V=128256 K=32768 fp32 logits; "
-                                   "reference step = one sequence of the batch through the CPU oracle",
-                       "global_batch": 1, "seq_len": GAMMA + 1, "parallelism": "replicas"},
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_text(), "global_batch": B, "seq_len": GAMMA + 1,
+                       "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": max(1, round(cpu / wall)),
                              "kind": "oracle",
-                             "sample": f"{args.steps} sequences, one per step"},
+                             "sample": f"{args.steps} samples; " + ORACLE_SAMPLE_TEXT},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
+def workload_text():
+    return ("speculative block with VocabTrim calibration: calibrate 50M Zipf(1.1) ids -> "
+            "Top-32768 of V=128256, trim W[128256,2048] bf16, 6 drafter steps B=16, "
+            "verify B=16 gamma=6 fp32 logits N(0,2)+3 ln Zipf_1.1 rank bias, T=1")
+
+
+# ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -256,33 +374,32 @@ def main():
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    else:
-        dist = None
 
     import __graft_entry__
     __graft_entry__.build()
     import drafter_sampling_gb300 as vt
 
-    per_set = VerifyStep.algorithmic_bytes()
-    nsets = max(2, int(np.ceil(4 * L2_BYTES / per_set)) + 1)
-    step = VerifyStep(torch, vt, dev, nsets)
+    host = HostInputs()
+    # every step streams ~1.3 GB (ids, W, W_trim, logits), far more than L2,
+    # so no input is L2-resident when the next step reads it; the logits also
+    # rotate between two buffers
+    step = GpuStep(torch, vt, dev, host, nsets=2)
     stream = torch.cuda.current_stream()
-
     for k in range(max(3, args.warmup)):
-        step.call(step.sets[k % nsets])
+        step.run(k)
     torch.cuda.synchronize()
 
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
-    clocks = ClockSampler(gpu_index)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    clocks = ClockSampler(int(vis) if vis.isdigit() else local)
     clocks.start()
     time.sleep(0.3)
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    nev = {"calibrate": 2, "trim": 2, "draft": 2 * GAMMA, "verify": 2}
+    events = [{r: [torch.cuda.Event(enable_timing=True) for _ in range(nev[r])] for r in ROWS}
+              for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -291,9 +408,7 @@ def main():
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(args.steps):
-        ev[k][0].record(stream)
-        step.call(step.sets[k % nsets])
-        ev[k][1].record(stream)
+        step.run(k, events[k])
     end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -301,89 +416,113 @@ def main():
         dist.barrier()
     clocks.stop()
     total_ms = start.elapsed_time(end)
-    call_ms = [a.elapsed_time(b) for a, b in ev]
     if dist is not None:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    units = B * GAMMA * args.steps * world
-    value = units / (total_ms / 1e3)
+    value = B * GAMMA * args.steps * world / (total_ms / 1e3)
+    status = [int(x) for x in step.status.cpu().tolist()]
 
-    status = int(step.status.item())
-
-    # e2e through the public API with host buffers (pinned), copies inside the timer
-    h = step.host
-    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in
-              dict(logits=h["logits"], q=h["q"], draft=h["draft"], u_acc=h["u_accept"],
-                   u_res=h["u_resample"]).items()}
-    out_host = torch.empty((B * (GAMMA + 1) + B,), dtype=torch.int32).pin_memory()
-    dsets = step.sets
-    e2e_steps = max(1, min(args.steps, 400))
-    for k in range(3):
-        s = dsets[k % nsets]
-        for key in pinned:
-            s[key].copy_(pinned[key], non_blocking=True)
-        step.call(s)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(e2e_steps):
-        s = dsets[k % nsets]
-        for key in pinned:
-            s[key].copy_(pinned[key], non_blocking=True)
-        step.call(s)
-        out_host[: B * (GAMMA + 1)].copy_(step.out_tokens.view(-1), non_blocking=True)
-        out_host[B * (GAMMA + 1):].copy_(step.out_n, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = B * GAMMA * e2e_steps * world / (e2e_ms / 1e3)
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = out_host.numel() * 4
-
+    # per-row durations from the events around each call
+    call_us = {r: [] for r in ROWS}
+    for ev in events:
+        for r in ROWS:
+            e = ev[r]
+            for i in range(0, len(e), 2):
+                call_us[r].append(e[i].elapsed_time(e[i + 1]) * 1e3)
     peak, peak_kind = peaks()
-    avg_call_ms = float(np.mean(call_ms))
-    alg = VerifyStep.algorithmic_bytes()
-    achieved = alg / (avg_call_ms / 1e3) / 1e9
-    traffic = traffic_for("vt_verify", ["drafter_sampling_gb300/csrc/vt_verify.cu",
-                                        "drafter_sampling_gb300/csrc/vt_common.cuh"])
+    alg = algorithmic_bytes()
+    rows = {}
+    for r in ROWS:
+        avg = float(np.mean(call_us[r]))
+        ach = alg[r] / (avg * 1e-6) / 1e9
+        rows[r] = {"calls_per_step": CALLS_PER_STEP[r], "avg_call_us": avg,
+                   "algorithmic_bytes": alg[r], "achieved_gbs": ach, "frac": ach / peak,
+                   "traffic": traffic_for(r), "kernels_per_call": KERNELS_PER_CALL[r]}
+    dominant = max(ROWS, key=lambda r: rows[r]["avg_call_us"] * CALLS_PER_STEP[r])
+    dom = rows[dominant]
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "batched verify B=16 gamma=6 V=128256 K=32768 fp32 logits "
-                               "(N(0,2) + 3 ln Zipf_1.1 rank bias)",
-                   "global_batch": B * world, "seq_len": GAMMA + 1,
+        "config": {"workload": workload_text(), "global_batch": B * world, "seq_len": GAMMA + 1,
                    "parallelism": f"replicas x{world}",
-                   "l2": f"rotating {nsets} input sets ({nsets * per_set / 1e6:.0f} MB > 4x L2)"},
-        "roofline": {"bound": "hbm", "kernel": "vt_verify (verify_stats + verify_finish)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes": alg, "avg_launch_us": avg_call_ms * 1e3,
-                     "peak_source": f"{peak_kind} hbm_gbs"},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": VerifyStep.kernels_per_step * args.steps,
+                   "l2": "each step streams >1.3 GB (>4x L2) of distinct inputs; logits "
+                         "rotate over 2 buffers"},
+        "roofline": {"bound": "hbm", "kernel": f"vt_{dominant} (dominant row)",
+                     "achieved": dom["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": dom["achieved_gbs"] / peak, "traffic": dom["traffic"],
+                     "algorithmic_bytes": dom["algorithmic_bytes"],
+                     "avg_launch_us": dom["avg_call_us"],
+                     "peak_source": f"{peak_kind} hbm_gbs (copy, of measured)"},
+        "rows": rows,
+        "verify_only": {"value": B * GAMMA / (rows["verify"]["avg_call_us"] * 1e-6),
+                        "unit": UNIT},
+        "gpu_launches": sum(KERNELS_PER_CALL[r] * CALLS_PER_STEP[r] for r in ROWS) * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "dev_status": status,
     }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(torch, step, host, stream, args, dist, dev, world)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_verify()
+        n, per_step, wall, cores, per_row = run_oracle_for(12.0, host)
+        line["cpu_baseline"] = {"value": B * GAMMA / per_step, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{n} samples in {wall:.1f} s; " + ORACLE_SAMPLE_TEXT,
+                                "est_s_per_step": per_row}
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
     return 0
+
+
+def run_e2e(torch, step, host, stream, args, dist, dev, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the verified tokens back."""
+    inp = host.step_inputs()
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in inp.items()}
+    dst = {"ids": step.ids, "W": step.W, "hidden": step.hidden, "u_draft": step.u_draft}
+    out_host = torch.empty(B * (GAMMA + 1) + B, dtype=torch.int32).pin_memory()
+    nsteps = max(1, min(args.steps, 50))
+
+    def one(k):
+        s = step.vsets[k % step.nsets]
+        for key, d in dst.items():
+            src = pinned[key]
+            d.copy_(src.view(d.dtype) if src.dtype != d.dtype else src, non_blocking=True)
+        s["logits"].copy_(pinned["logits"], non_blocking=True)
+        s["u_acc"].copy_(pinned["u_accept"], non_blocking=True)
+        s["u_res"].copy_(pinned["u_resample"], non_blocking=True)
+        step.run(k)
+        out_host[: B * (GAMMA + 1)].copy_(step.out_tokens.view(-1), non_blocking=True)
+        out_host[B * (GAMMA + 1):].copy_(step.out_n, non_blocking=True)
+
+    for k in range(2):
+        one(k)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(nsteps):
+        one(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    return {"value": B * GAMMA * nsteps * world / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * 4,
+            "steps": nsteps}
 
 
 if __name__ == "__main__":

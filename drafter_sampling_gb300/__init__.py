@@ -67,6 +67,8 @@ def workspace_bytes(kind: str, **kw) -> int:
     L = lib()
     if kind == "calibrate":
         return L.vt_calibrate_topk_workspace_bytes(kw["n"], kw["V"], kw["K"])
+    if kind == "trim":
+        return L.vt_trim_head_workspace_bytes(kw["V"], kw["K"])
     if kind == "draft":
         return L.vt_draft_workspace_bytes(kw["B"], kw["H"], kw["K"])
     if kind == "verify":
@@ -105,7 +107,7 @@ def vt_calibrate_topk(ids, V: int, K: int, counts=None, topk_ids=None, dev_statu
 
 
 def vt_trim_head(W, topk_ids, W_trim=None, trim_ids=None, inv_map=None, dev_status=None,
-                 stream=None):
+                 workspace=None, stream=None):
     """W_trim = W[sorted(topk_ids)], trim_ids (ascending) and inv_map.
 
     Returns (W_trim [K,H] same dtype as W, trim_ids int32 [K], inv_map int32 [V], dev_status).
@@ -127,9 +129,12 @@ def vt_trim_head(W, topk_ids, W_trim=None, trim_ids=None, inv_map=None, dev_stat
     _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
     if tuple(W_trim.shape) != (K, H) or trim_ids.numel() != K or inv_map.numel() != V:
         raise ValueError("output shapes do not match (K, H), K and V")
-    st = lib().vt_trim_head(W.data_ptr(), V, H, topk_ids.data_ptr(), K, W_trim.data_ptr(),
-                            trim_ids.data_ptr(), inv_map.data_ptr(), dev_status.data_ptr(),
-                            _stream_ptr(stream))
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_trim_head_workspace_bytes(V, K), dev)
+    st = L.vt_trim_head(W.data_ptr(), V, H, topk_ids.data_ptr(), K, W_trim.data_ptr(),
+                        trim_ids.data_ptr(), inv_map.data_ptr(), dev_status.data_ptr(),
+                        workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _lib.check("vt_trim_head", st)
     return W_trim, trim_ids, inv_map, dev_status
 
@@ -160,10 +165,11 @@ def vt_draft_logits(hidden, W_trim, temperature: float = 1.0, logits=None, works
 
 def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, q=None,
                   tokens=None, dev_status=None, workspace=None, stream=None):
-    """One drafting step; returns (q [B, K] view, tokens int32 [B], dev_status).
+    """One drafting step; returns (q [B, K] view, tokens int32 [B] view, dev_status).
 
     ``q`` may be a strided view such as q_all[:, pos, :] of a contiguous
-    [B, gamma, K] tensor (unit inner stride).
+    [B, gamma, K] tensor (unit inner stride), and ``tokens`` a strided view
+    such as tok_all[:, pos] of a [B, gamma] tensor.
     """
     torch = _torch()
     _dev(hidden, "hidden", _bf16_dtypes(), 2)
@@ -179,6 +185,8 @@ def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, 
         raise ValueError("q must be [B, K] with unit inner stride")
     if tokens is None:
         tokens = torch.empty(B, dtype=torch.int32, device=dev)
+    if tokens.dim() != 1 or tokens.shape[0] != B or tokens.dtype != torch.int32:
+        raise ValueError("tokens must be an int32 vector of B entries (any stride)")
     if dev_status is None:
         dev_status = torch.empty(1, dtype=torch.int32, device=dev)
     if uniforms.numel() != B or trim_ids.numel() != K:
@@ -188,8 +196,8 @@ def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, 
         workspace = _ws(L.vt_draft_workspace_bytes(B, H, K), dev)
     st = L.vt_draft_step(hidden.data_ptr(), B, H, W_trim.data_ptr(), trim_ids.data_ptr(), K,
                          uniforms.data_ptr(), float(temperature), q.data_ptr(), q.stride(0),
-                         tokens.data_ptr(), dev_status.data_ptr(), workspace.data_ptr(),
-                         workspace.numel(), _stream_ptr(stream))
+                         tokens.data_ptr(), tokens.stride(0), dev_status.data_ptr(),
+                         workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _lib.check("vt_draft_step", st)
     return q, tokens, dev_status
 

@@ -42,11 +42,12 @@ SIGNATURES = {
     "vt_abi_version": (C.c_int, []),
     "vt_calibrate_topk_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "vt_calibrate_topk": (C.c_int, [_p, _i64, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
-    "vt_trim_head": (C.c_int, [_p, _i32, _i32, _p, _i32, _p, _p, _p, _p, _p]),
+    "vt_trim_head_workspace_bytes": (_sz, [_i32, _i32]),
+    "vt_trim_head": (C.c_int, [_p, _i32, _i32, _p, _i32, _p, _p, _p, _p, _p, _sz, _p]),
     "vt_draft_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "vt_draft_logits": (C.c_int, [_p, _i32, _i32, _p, _i32, _f32, _p, _i64, _p, _sz, _p]),
-    "vt_draft_step": (C.c_int, [_p, _i32, _i32, _p, _p, _i32, _p, _f32, _p, _i64, _p, _p,
-                                _p, _sz, _p]),
+    "vt_draft_step": (C.c_int, [_p, _i32, _i32, _p, _p, _i32, _p, _f32, _p, _i64, _p, _i64,
+                                _p, _p, _sz, _p]),
     "vt_verify_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "vt_verify": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32, _p,
                             _p, _p, _p, _p, _sz, _p]),

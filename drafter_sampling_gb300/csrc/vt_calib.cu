@@ -8,16 +8,23 @@
 //    mapper T_{d->t} of Algorithm 2 and its inverse.
 //
 // Kernels:
-//  * hist:    grid-stride 16-byte loads of the id stream; lanes holding the
-//             same id merge their increments (match.any) before one atomic,
-//             so hot ids of a Zipf stream do not serialise a warp.
+//  * hist:    the Zipf head of a token stream would serialise a plain atomic
+//             histogram on a few addresses (the most frequent id alone is
+//             ~13% of the stream).  A sample of the first 256K ids picks the
+//             hot ids (sample count >= sample/4096); the main pass keeps a
+//             bitmap and a small hash table of them in shared memory and
+//             counts hot ids in per-CTA shared counters, cold ids with
+//             global atomics; lanes holding the same id merge first
+//             (match.any).  The sample only decides where an id is counted,
+//             so the counts are exact whatever it picks.
 //  * radix:   stable LSD radix sort of (~count, id) by 8-bit digits: per-tile
 //             digit counts, one exclusive scan, stable scatter.  Stability
 //             makes equal counts keep ascending id order, which is the tie
 //             rule.  Exact integer work: the result is bit-identical to a
 //             sequential sort.
-//  * trim:    mark the K ids in inv_map, one-block exclusive scan in id
-//             order (writes trim_ids and inv_map), row gather of W.
+//  * trim:    mark the K ids in inv_map, exclusive scan in id order (tile
+//             counts, then tile-local scans that write trim_ids and inv_map),
+//             row gather of W.
 #include <algorithm>
 
 #include "vt_common.cuh"
@@ -27,57 +34,134 @@ namespace {
 
 constexpr int kHistNT = 256;
 constexpr int kSortNT = 256;
-constexpr int kSortItems = 8;
+constexpr int kSortItems = 2;
 constexpr int kSortTile = kSortNT * kSortItems;
 constexpr int kScanNT = 1024;
+constexpr int kHotMax = 8192;            // hot ids counted in shared memory
+constexpr int64_t kSample = 1 << 17;     // ids in the hot-id sample
+constexpr unsigned kSampleThr = 2;       // sample count that makes an id hot
+constexpr int kHotBitmapMaxV = 1 << 19;  // bitmap + prefix of hot ids fit in 96 KB
 
-// ------------------------------------------------------------- histogram
-__device__ __forceinline__ void count_one(int id, int V, unsigned* counts, int& bad) {
-  const bool ok = (unsigned)id < (unsigned)V;
-  if (!ok) bad = 1;
-  const unsigned active = __activemask();
-  // group the lanes that hold the same valid id; out-of-range ids form their
-  // own groups keyed by a value no valid id can take
-  const int key = ok ? id : -1 - (int)(threadIdx.x & 31);
-  const unsigned peers = __match_any_sync(active, key);
-  const int leader = __ffs(peers) - 1;
-  if (ok && (int)(threadIdx.x & 31) == leader) atomicAdd(counts + id, (unsigned)__popc(peers));
+// sample histogram of the first `ns` ids (warp-aggregated global atomics)
+__global__ void __launch_bounds__(kHistNT)
+hist_sample_kernel(const int* __restrict__ ids, int64_t ns, int V, unsigned* __restrict__ tmp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * kHistNT;
+  for (int64_t i0 = (int64_t)blockIdx.x * kHistNT + threadIdx.x - lane; i0 < ns; i0 += stride) {
+    const int64_t i = i0 + lane;
+    const int id = (i < ns) ? __ldg(ids + i) : -1;
+    const bool ok = (unsigned)id < (unsigned)V;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
+    if (ok && lane == __ffs(peers) - 1) atomicAdd(tmp + id, (unsigned)__popc(peers));
+  }
 }
 
+// ids whose sample count reaches `thr` (at most kHotMax, any order)
+__global__ void hot_select_kernel(const unsigned* __restrict__ tmp, int V, unsigned thr,
+                                  int* __restrict__ hot_list, int* __restrict__ hot_n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < V && tmp[i] >= thr) {
+    const int slot = atomicAdd(hot_n, 1);
+    if (slot < kHotMax) hot_list[slot] = i;
+  }
+}
+
+// Hot ids: a bitmap over [0, V) in shared memory, and their slot = the rank
+// of their bit (per-word prefix counts + popc), so the shared counters are
+// indexed without a search.  Hot ids take shared atomics (contention stays
+// inside one SM); the rest take global atomics, where no address is hot.
 __global__ void __launch_bounds__(kHistNT)
-hist_kernel(const int* __restrict__ ids, int64_t n, int V, unsigned* __restrict__ counts,
-            int* __restrict__ dev_status, int vec_ok) {
+hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __restrict__ hot_list,
+                 const int* __restrict__ hot_n, unsigned* __restrict__ counts,
+                 int* __restrict__ dev_status, int vec_ok, int use_hot) {
+  extern __shared__ unsigned smem[];
+  const int nwords = (V + 31) / 32;
+  unsigned* bitmap = smem;                                              // [nwords]
+  unsigned short* prefix = reinterpret_cast<unsigned short*>(smem + nwords);  // [nwords]
+  unsigned* hcnt = smem + nwords + (nwords + 1) / 2;                    // [kHotMax]
+  __shared__ int wsum[kHistNT / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (use_hot) {
+    for (int w = tid; w < nwords; w += kHistNT) bitmap[w] = 0;
+    for (int h = tid; h < kHotMax; h += kHistNT) hcnt[h] = 0;
+    __syncthreads();
+    const int nh = min(*hot_n, kHotMax);
+    for (int sl = tid; sl < nh; sl += kHistNT) {
+      const int id = hot_list[sl];
+      atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+    }
+    __syncthreads();
+    // prefix[w] = number of hot ids in words before w
+    const int per = (nwords + kHistNT - 1) / kHistNT;
+    const int w0 = tid * per, w1 = min(nwords, w0 + per);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bitmap[w]);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int run = x - c;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int w = w0; w < w1; ++w) {
+      prefix[w] = (unsigned short)run;
+      run += __popc(bitmap[w]);
+    }
+    __syncthreads();
+  }
   int bad = 0;
+  auto count = [&](int id) {
+    if ((unsigned)id >= (unsigned)V) {
+      bad = 1;
+      return;
+    }
+    if (use_hot) {
+      const unsigned word = bitmap[id >> 5];
+      const unsigned bit = 1u << (id & 31);
+      if (word & bit) {
+        atomicAdd(&hcnt[prefix[id >> 5] + __popc(word & (bit - 1))], 1u);
+        return;
+      }
+    }
+    atomicAdd(counts + id, 1u);
+  };
   const int64_t stride = (int64_t)gridDim.x * kHistNT;
-  const int64_t t0 = (int64_t)blockIdx.x * kHistNT + threadIdx.x;
+  const int64_t t0 = (int64_t)blockIdx.x * kHistNT + tid;
   int64_t tail_start = 0;
   if (vec_ok) {
     const int64_t nv = n / 4;
     const int4* v4 = reinterpret_cast<const int4*>(ids);
-    // every lane of a warp runs the same number of iterations so match.any
-    // sees full warps; lanes past the end use the sentinel
-    const int64_t warp_base = t0 - (threadIdx.x & 31);
-    for (int64_t i0 = warp_base; i0 < nv; i0 += stride) {
-      const int64_t i = i0 + (threadIdx.x & 31);
-      int4 v = make_int4(0, 0, 0, 0);
-      const bool in = i < nv;
-      if (in) v = __ldg(v4 + i);
-      const int vals[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int id = vals[k];
-        const bool ok = in && (unsigned)id < (unsigned)V;
-        if (in && !ok) bad = 1;
-        const int key = ok ? id : -1 - (int)(threadIdx.x & 31);
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (ok && (int)(threadIdx.x & 31) == __ffs(peers) - 1)
-          atomicAdd(counts + id, (unsigned)__popc(peers));
-      }
+    int64_t i = t0;
+    for (; i + stride < nv; i += 2 * stride) {
+      const int4 a = __ldg(v4 + i), b = __ldg(v4 + i + stride);
+      count(a.x); count(a.y); count(a.z); count(a.w);
+      count(b.x); count(b.y); count(b.z); count(b.w);
+    }
+    if (i < nv) {
+      const int4 a = __ldg(v4 + i);
+      count(a.x); count(a.y); count(a.z); count(a.w);
     }
     tail_start = nv * 4;
   }
-  for (int64_t i = tail_start + t0; i < n; i += stride) count_one(__ldg(ids + i), V, counts, bad);
+  for (int64_t i = tail_start + t0; i < n; i += stride) count(__ldg(ids + i));
   if (bad) atomicOr(dev_status, VT_DEV_BAD_ID);
+  if (use_hot) {
+    __syncthreads();
+    // flush: each set bit of the bitmap is one hot id with its slot
+    for (int w = tid; w < nwords; w += kHistNT) {
+      unsigned word = bitmap[w];
+      int slot = prefix[w];
+      while (word) {
+        const int b = __ffs(word) - 1;
+        word &= word - 1;
+        const unsigned c = hcnt[slot++];
+        if (c) atomicAdd(counts + w * 32 + b, c);
+      }
+    }
+  }
 }
 
 // ----------------------------------------------------------- radix sort
@@ -106,43 +190,65 @@ sort_count_kernel(const unsigned* __restrict__ keys, int V, int shift, int ntile
   ghist[threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
 }
 
-// exclusive scan of n ints in place, one block
-__global__ void __launch_bounds__(kScanNT) scan_ints_kernel(int* __restrict__ a, int n) {
+// exclusive scan of ghist in blocks of kScanBlock entries: each block scans
+// its entries in place (block-local offsets) and writes its total; the
+// scatter kernel adds the totals of the blocks before.
+constexpr int kScanBlock = kScanNT * 4;
+
+__global__ void __launch_bounds__(kScanNT)
+scan_blocks_kernel(int* __restrict__ a, int n, int* __restrict__ btot) {
   __shared__ int wsum[kScanNT / 32];
-  const int per = (n + kScanNT - 1) / kScanNT;
-  const int s = threadIdx.x * per;
-  const int e = min(n, s + per);
-  int local = 0;
-  for (int i = s; i < e; ++i) local += a[i];
-  // block exclusive scan of `local`
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = local;
+  const int64_t j = (int64_t)blockIdx.x * kScanBlock + 4 * threadIdx.x;
+  int v[4], c = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[e] = (j + e < n) ? a[j + e] : 0;
+    c += v[e];
+  }
+  int x = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
-  int wpre = 0;
-  for (int w = 0; w < warp; ++w) wpre += wsum[w];
-  int run = wpre + x - local;
-  for (int i = s; i < e; ++i) {
-    const int v = a[i];
-    a[i] = run;
-    run += v;
+  int run = x - c, tot = 0;
+  for (int w = 0; w < kScanNT / 32; ++w) {
+    if (w < warp) run += wsum[w];
+    tot += wsum[w];
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (j + e < n) a[j + e] = run;
+    run += v[e];
+  }
+  if (threadIdx.x == 0) btot[blockIdx.x] = tot;
 }
 
 __global__ void __launch_bounds__(kSortNT)
 sort_scatter_kernel(const unsigned* __restrict__ keys_in, const int* __restrict__ vals_in, int V,
                     int shift, int ntiles, const int* __restrict__ goff,
+                    const int* __restrict__ btot, int nblk,
                     unsigned* __restrict__ keys_out, int* __restrict__ vals_out) {
   __shared__ int base_d[256];
   __shared__ int cnt_d[256];
   __shared__ int wc[kSortNT / 32][256];
+  __shared__ int bpre[64];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  base_d[tid] = goff[tid * ntiles + blockIdx.x];
+  if (tid == 0) {
+    int r = 0;
+    for (int k = 0; k < nblk; ++k) {
+      bpre[k] = r;
+      r += btot[k];
+    }
+  }
+  __syncthreads();
+  {
+    const int e = tid * ntiles + blockIdx.x;
+    base_d[tid] = goff[e] + bpre[e / kScanBlock];
+  }
   cnt_d[tid] = 0;
   const int64_t base = (int64_t)blockIdx.x * kSortTile;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -180,6 +286,20 @@ sort_scatter_kernel(const unsigned* __restrict__ keys_in, const int* __restrict_
   }
 }
 
+// zero the counts, the sample histogram, the hot-id count and the status
+__global__ void calib_zero_kernel(unsigned* __restrict__ counts, unsigned* __restrict__ tmp, int V,
+                                  int* __restrict__ hot_n, int* __restrict__ dev_status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < V) {
+    counts[i] = 0;
+    tmp[i] = 0;
+  }
+  if (i == 0) {
+    *hot_n = 0;
+    *dev_status = 0;
+  }
+}
+
 __global__ void copy_ints_kernel(const int* __restrict__ src, int* __restrict__ dst, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = src[i];
@@ -198,45 +318,88 @@ __global__ void trim_mark_kernel(const int* __restrict__ topk, int K, int V,
   if (atomicAdd(flags + id, 1) != 0) atomicOr(dev_status, VT_DEV_DUPLICATE_ID);
 }
 
-// flags[id] != 0 marks a kept id.  One block scans in id order and writes
+// flags[id] != 0 marks a kept id.  Two passes over tiles of kTrimTile ids:
+// count the kept ids of each tile, then every tile adds the counts of the
+// tiles before it, scans its own flags in id order and writes
 // trim_ids[pos] = id and inv_map[id] = pos (or -1), in place over flags.
-__global__ void __launch_bounds__(kScanNT)
-trim_scan_kernel(int* __restrict__ inv_map, int V, int K, int* __restrict__ trim_ids) {
-  __shared__ int wsum[kScanNT / 32];
-  __shared__ int s_total;
-  const int per = (V + kScanNT - 1) / kScanNT;
-  const int s = threadIdx.x * per;
-  const int e = min(V, s + per);
-  int local = 0;
-  for (int i = s; i < e; ++i) local += (inv_map[i] != 0);
+constexpr int kTrimNT = 256;
+constexpr int kTrimTile = kTrimNT * 4;
+
+__device__ __forceinline__ int block_excl_scan_int(int v, int* wsum, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = local;
+  int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
-  int wpre = 0, tot = 0;
-  for (int w = 0; w < kScanNT / 32; ++w) {
-    if (w < warp) wpre += wsum[w];
+  int pre = 0, tot = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    if (w < warp) pre += wsum[w];
     tot += wsum[w];
   }
-  if (threadIdx.x == 0) s_total = tot;
-  int run = wpre + x - local;
-  for (int i = s; i < e; ++i) {
-    if (inv_map[i] != 0) {
-      if (run < K) trim_ids[run] = i;
-      inv_map[i] = (run < K) ? run : -1;
-      ++run;
-    } else {
-      inv_map[i] = -1;
-    }
+  __syncthreads();
+  total = tot;
+  return pre + x - v;
+}
+
+__global__ void __launch_bounds__(kTrimNT)
+trim_tilecount_kernel(const int* __restrict__ flags, int V, int* __restrict__ tcount) {
+  __shared__ int wsum[kTrimNT / 32];
+  const int64_t j = (int64_t)blockIdx.x * kTrimTile + 4 * threadIdx.x;
+  int c = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) c += (j + e < V && flags[j + e] != 0);
+  int total;
+  block_excl_scan_int(c, wsum, total);
+  if (threadIdx.x == 0) tcount[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kTrimNT)
+trim_write_kernel(int* __restrict__ inv_map, int V, int K, const int* __restrict__ tcount,
+                  int ntiles, int* __restrict__ trim_ids) {
+  __shared__ int wsum[kTrimNT / 32];
+  __shared__ int s_pre, s_all;
+  // kept ids in the tiles before this one, and in all tiles
+  int pre = 0, all = 0;
+  for (int t = threadIdx.x; t < ntiles; t += kTrimNT) {
+    const int c = tcount[t];
+    if (t < (int)blockIdx.x) pre += c;
+    all += c;
+  }
+  int tp, ta;
+  block_excl_scan_int(pre, wsum, tp);
+  block_excl_scan_int(all, wsum, ta);
+  if (threadIdx.x == 0) {
+    s_pre = tp;
+    s_all = ta;
   }
   __syncthreads();
+  const int64_t j = (int64_t)blockIdx.x * kTrimTile + 4 * threadIdx.x;
+  int f[4], c = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[e] = (j + e < V) ? (inv_map[j + e] != 0) : 0;
+    c += f[e];
+  }
+  int total;
+  int run = s_pre + block_excl_scan_int(c, wsum, total);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (j + e >= V) break;
+    if (f[e]) {
+      if (run < K) trim_ids[run] = (int)(j + e);
+      inv_map[j + e] = (run < K) ? run : -1;
+      ++run;
+    } else {
+      inv_map[j + e] = -1;
+    }
+  }
   // fewer than K distinct ids (bad input): pad trim_ids
-  for (int p = s_total + threadIdx.x; p < K; p += kScanNT) trim_ids[p] = -1;
+  if (blockIdx.x == 0)
+    for (int p = s_all + threadIdx.x; p < K; p += kTrimNT) trim_ids[p] = -1;
 }
 
 // one warp per trimmed row: W_trim[j, :] = W[trim_ids[j], :]
@@ -273,6 +436,10 @@ struct CalibWs {
   unsigned* keys[2];
   int* vals[2];
   int* ghist;
+  int* btot;       // [64] block totals of the offset scan
+  unsigned* tmp;   // sample histogram [V]
+  int* hot_list;   // [kHotMax]
+  int* hot_n;      // [1]
   size_t bytes;
 };
 
@@ -288,7 +455,15 @@ CalibWs carve_calib(void* base, int V) {
   size_t k0 = take((size_t)V * 4), k1 = take((size_t)V * 4);
   size_t v0 = take((size_t)V * 4), v1 = take((size_t)V * 4);
   size_t gh = take((size_t)256 * ntiles * 4);
+  size_t bt = take(64 * 4);
+  size_t tm = take((size_t)V * 4);
+  size_t hl = take((size_t)kHotMax * 4);
+  size_t hn = take(4);
   char* p = static_cast<char*>(base);
+  w.btot = reinterpret_cast<int*>(p + bt);
+  w.tmp = reinterpret_cast<unsigned*>(p + tm);
+  w.hot_list = reinterpret_cast<int*>(p + hl);
+  w.hot_n = reinterpret_cast<int*>(p + hn);
   w.keys[0] = reinterpret_cast<unsigned*>(p + k0);
   w.keys[1] = reinterpret_cast<unsigned*>(p + k1);
   w.vals[0] = reinterpret_cast<int*>(p + v0);
@@ -331,27 +506,47 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  VT_RETURN_IF_CUDA(cudaMemsetAsync(counts, 0, (size_t)V * 4, s));
-  VT_RETURN_IF_CUDA(cudaMemsetAsync(dev_status, 0, 4, s));
+  calib_zero_kernel<<<(V + 255) / 256, 256, 0, s>>>(counts, ws.tmp, V, ws.hot_n, dev_status);
+  VT_RETURN_IF_LAUNCH_FAILED();
   if (n > 0) {
     const int vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
-    int64_t want = (n / 4 + kHistNT - 1) / kHistNT;
-    int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
-    hist_kernel<<<grid, kHistNT, 0, s>>>(ids, n, V, counts, dev_status, vec_ok);
+    const int use_hot = V <= kHotBitmapMaxV;
+    if (use_hot) {
+      const int64_t ns = std::min<int64_t>(n, kSample);
+      const unsigned thr = kSampleThr;
+      hist_sample_kernel<<<(unsigned)((ns + kHistNT - 1) / kHistNT), kHistNT, 0, s>>>(ids, ns, V,
+                                                                                   ws.tmp);
+      VT_RETURN_IF_LAUNCH_FAILED();
+      hot_select_kernel<<<(V + 255) / 256, 256, 0, s>>>(ws.tmp, V, thr, ws.hot_list, ws.hot_n);
+      VT_RETURN_IF_LAUNCH_FAILED();
+    }
+    const int nwords = (V + 31) / 32;
+    const size_t smem = use_hot ? ((size_t)nwords + (nwords + 1) / 2 + kHotMax) * 4 : 0;
+    if (smem > 48 * 1024)
+      VT_RETURN_IF_CUDA(cudaFuncSetAttribute(hist_main_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem));
+    const int64_t want = (n / 4 + kHistNT - 1) / kHistNT;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
+    hist_main_kernel<<<grid, kHistNT, smem, s>>>(ids, n, V, ws.hot_list, ws.hot_n, counts,
+                                                 dev_status, vec_ok, use_hot);
     VT_RETURN_IF_LAUNCH_FAILED();
   }
   sort_init_kernel<<<(V + 255) / 256, 256, 0, s>>>(counts, V, ws.keys[0], ws.vals[0]);
   VT_RETURN_IF_LAUNCH_FAILED();
   const int ntiles = (V + kSortTile - 1) / kSortTile;
+  const int nblk = (256 * ntiles + kScanBlock - 1) / kScanBlock;
+  if (nblk > 64) return VT_ERR_UNSUPPORTED;
   int cur = 0;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 8 * pass;
     sort_count_kernel<<<ntiles, kSortNT, 0, s>>>(ws.keys[cur], V, shift, ntiles, ws.ghist);
     VT_RETURN_IF_LAUNCH_FAILED();
-    scan_ints_kernel<<<1, kScanNT, 0, s>>>(ws.ghist, 256 * ntiles);
+    scan_blocks_kernel<<<nblk, kScanNT, 0, s>>>(ws.ghist, 256 * ntiles, ws.btot);
     VT_RETURN_IF_LAUNCH_FAILED();
     sort_scatter_kernel<<<ntiles, kSortNT, 0, s>>>(ws.keys[cur], ws.vals[cur], V, shift, ntiles,
-                                                   ws.ghist, ws.keys[cur ^ 1], ws.vals[cur ^ 1]);
+                                                   ws.ghist, ws.btot, nblk, ws.keys[cur ^ 1],
+                                                   ws.vals[cur ^ 1]);
     VT_RETURN_IF_LAUNCH_FAILED();
     cur ^= 1;
   }
@@ -360,18 +555,31 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
   return VT_OK;
 }
 
+extern "C" size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K) {
+  (void)K;
+  if (V < 1) return 0;
+  return vt::align_up((size_t)((V + vt::kTrimTile - 1) / vt::kTrimTile) * 4, 256);
+}
+
 extern "C" int vt_trim_head(const uint16_t* W, int32_t V, int32_t H, const int32_t* topk_ids,
                             int32_t K, uint16_t* W_trim, int32_t* trim_ids, int32_t* inv_map,
-                            int32_t* dev_status, void* stream) {
+                            int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   using namespace vt;
   if (!W || !topk_ids || !W_trim || !trim_ids || !inv_map || !dev_status) return VT_ERR_INVALID_ARG;
-  if (V < 1 || H < 1 || K < 1 || K > V) return VT_ERR_INVALID_ARG;
+  if (V < 1 || V > (1 << 30) || H < 1 || K < 1 || K > V) return VT_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
+  if (workspace_bytes < vt_trim_head_workspace_bytes(V, K)) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   VT_RETURN_IF_CUDA(cudaMemsetAsync(inv_map, 0, (size_t)V * 4, s));
   VT_RETURN_IF_CUDA(cudaMemsetAsync(dev_status, 0, 4, s));
   trim_mark_kernel<<<(K + 255) / 256, 256, 0, s>>>(topk_ids, K, V, inv_map, dev_status);
   VT_RETURN_IF_LAUNCH_FAILED();
-  trim_scan_kernel<<<1, kScanNT, 0, s>>>(inv_map, V, K, trim_ids);
+  const int ntiles = (V + kTrimTile - 1) / kTrimTile;
+  int* tcount = static_cast<int*>(workspace);  // kept-id count of each tile
+  trim_tilecount_kernel<<<ntiles, kTrimNT, 0, s>>>(inv_map, V, tcount);
+  VT_RETURN_IF_LAUNCH_FAILED();
+  trim_write_kernel<<<ntiles, kTrimNT, 0, s>>>(inv_map, V, K, tcount, ntiles, trim_ids);
   VT_RETURN_IF_LAUNCH_FAILED();
   const int vec_ok = (H % 8 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(W_trim) & 15) == 0);

@@ -199,6 +199,7 @@ struct FinArgs {
   const float* u;
   const int* trim_ids;
   int* tokens;
+  int64_t ldt;
   float* zpart;
   int* lpart;
   int nchunk;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   v = block_ms_reduce<kFinNT>(v, mred);
   if (!(v.s > 0.f && isfinite(v.s) && isfinite(v.m))) {
     if (c == 0 && tid == 0) {
-      a.tokens[b] = -1;
+      a.tokens[(int64_t)b * a.ldt] = -1;
       atomicOr(a.dev_status, VT_DEV_NONFINITE);
     }
     return;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     pick = (s_pick >= 0) ? s_pick : (lp2 >= 0 ? lp2 : pick);
   }
   if (tid == 0) {
-    a.tokens[b] = (pick >= 0) ? a.trim_ids[pick] : -1;
+    a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
     a.counters[b] = 0;
   }
 }
@@ -476,12 +477,13 @@ extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
 extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                              const uint16_t* W_trim, const int32_t* trim_ids, int32_t K,
                              const float* uniforms, float temperature, float* q, int64_t ldq,
-                             int32_t* tokens, int32_t* dev_status, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             int32_t* tokens, int64_t ld_tokens, int32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   using namespace vt;
   int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
   if (st != VT_OK) return st;
-  if (!trim_ids || !uniforms || !q || ldq < K || !tokens || !dev_status) return VT_ERR_INVALID_ARG;
+  if (!trim_ids || !uniforms || !q || ldq < K || !tokens || ld_tokens < 1 || !dev_status)
+    return VT_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   DraftWs ws = carve_draft(workspace, B);
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
@@ -502,6 +504,7 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   fa.u = uniforms;
   fa.trim_ids = trim_ids;
   fa.tokens = tokens;
+  fa.ldt = ld_tokens;
   fa.zpart = ws.zpart;
   fa.lpart = ws.lpart;
   int nchunk = (num_sms() * 4 + B - 1) / B;

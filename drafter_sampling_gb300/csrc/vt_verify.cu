@@ -304,7 +304,7 @@ __device__ int select_in_tile(const VArgs& a, const T* rowp, const float* qrow, 
 
 // -------------------------------------------------------------- kernel 2
 template <typename T>
-__global__ void __launch_bounds__(kNT) verify_finish_kernel(VArgs a) {
+__global__ void __launch_bounds__(kNT, 8) verify_finish_kernel(VArgs a) {
   __shared__ Smem sm;
   const int b = blockIdx.x, c = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -110,12 +110,14 @@ int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
  *  trim_ids  int32 [K]       out: the selected ids, ascending (T_{d->t})
  *  inv_map   int32 [V]       out: inv_map[trim_ids[j]] = j, -1 elsewhere
  *  dev_status int32 [1]      out: VT_DEV_BAD_ID / VT_DEV_DUPLICATE_ID
- * Needs no workspace.
+ * Workspace: vt_trim_head_workspace_bytes(V, K) bytes (4 bytes per 1024 ids).
  * ---------------------------------------------------------------------- */
+size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K);
 int vt_trim_head(const uint16_t* W, int32_t V, int32_t H,
                  const int32_t* topk_ids, int32_t K,
                  uint16_t* W_trim, int32_t* trim_ids, int32_t* inv_map,
-                 int32_t* dev_status, void* stream);
+                 int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                 void* stream);
 
 /* ------------------------------------------------------------------------
  * Drafter logits through the trimmed head.  [VT] Algorithm 2, drafting
@@ -149,14 +151,17 @@ int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
  *  q         f32  [B, ldq]   out: q[b, j] for j < K (ldq >= K; pass
  *                            ldq = gamma*K and q + pos*K to fill position
  *                            `pos` of a [B, gamma, K] tensor)
- *  tokens    int32 [B]       out: drafted target ids
+ *  tokens    int32 [B, ld_tokens] out: drafted target ids in column 0
+ *                            (pass ld_tokens = gamma and tokens + pos to fill
+ *                            column `pos` of a [B, gamma] tensor; ld_tokens >= 1)
  *  dev_status int32 [1]      out: VT_DEV_NONFINITE
  * ---------------------------------------------------------------------- */
 int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                   const uint16_t* W_trim, const int32_t* trim_ids, int32_t K,
                   const float* uniforms, float temperature,
-                  float* q, int64_t ldq, int32_t* tokens, int32_t* dev_status,
-                  void* workspace, size_t workspace_bytes, void* stream);
+                  float* q, int64_t ldq, int32_t* tokens, int64_t ld_tokens,
+                  int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                  void* stream);
 
 /* ------------------------------------------------------------------------
  * Batched block verification by modified rejection sampling.

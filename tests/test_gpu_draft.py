@@ -119,17 +119,23 @@ def test_full_vocab_head_and_trimmed_consistency(vt):
     assert_probs_close(qt.cpu().numpy(), masked, "trimmed vs restricted full head")
 
 
-def test_q_written_into_a_position_of_a_block_tensor(vt):
+def test_q_and_tokens_written_into_a_position_of_block_tensors(vt):
     B, H, K, gamma, pos = 4, 64, 500, 5, 2
     hidden, W, trim_ids, u = _head(B, H, K, seed=3)
     q_all = torch.full((B, gamma, K), -5.0, dtype=torch.float32, device="cuda")
-    vt.vt_draft_step(_bf(hidden), _bf(W), _dev(trim_ids), _dev(u), 1.0, q=q_all[:, pos, :])
+    t_all = torch.full((B, gamma), -5, dtype=torch.int32, device="cuda")
+    vt.vt_draft_step(_bf(hidden), _bf(W), _dev(trim_ids), _dev(u), 1.0, q=q_all[:, pos, :],
+                     tokens=t_all[:, pos])
     torch.cuda.synchronize()
     ref = oracle.draft_step(hidden, W, trim_ids, u, 1.0)
     qa = q_all.cpu().numpy()
     assert_probs_close(qa[:, pos, :], ref["q"], "q slice")
-    others = np.delete(qa, pos, axis=1)
-    assert np.all(others == -5.0)
+    assert np.all(np.delete(qa, pos, axis=1) == -5.0)
+    ta = t_all.cpu().numpy()
+    for b in range(B):
+        if ref["margin"][b] > BOUNDARY:
+            assert ta[b, pos] == ref["tokens"][b]
+    assert np.all(np.delete(ta, pos, axis=1) == -5)
 
 
 def test_one_hot_hidden_gives_exact_logits(vt):
