@@ -9,7 +9,10 @@
 //   CDF of q[b] at u_b in ascending j (ascending target id).
 //
 // Kernels:
-//  1. draft_gemv: streams W_trim once from HBM with 16-byte loads, four lanes
+//  1. the projection, on the tensor cores when the shapes allow it
+//     (head_umma_kernel in vt_umma.cuh: tcgen05 MMA, TMA-fed, accumulator in
+//     tensor memory; batch <= 256, H a multiple of 8, 16-byte aligned rows),
+//     otherwise draft_gemv on the CUDA cores: it streams W_trim once from HBM with 16-byte loads, four lanes
 //     per row (64 contiguous bytes per row per step), the hidden tile in
 //     shared memory (broadcast reads), fp32 FMA accumulation.  Its epilogue
 //     stores z (scaled to base 2 for the softmax) and folds each CTA's rows
@@ -21,7 +24,10 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cudaTypedefs.h>
+
 #include "vt_common.cuh"
+#include "vt_umma.cuh"
 
 namespace vt {
 namespace {
@@ -369,10 +375,15 @@ struct DraftWs {
   float* zpart;
   int* lpart;
   int* counters;
+  int* status_sink;  // status word of calls that report none (vt_draft_logits)
   size_t bytes;
 };
 
-DraftWs carve_draft(void* base, int B) {
+int max_groups(int K) {
+  return std::max(kMaxGemvCtas, (K + umma::kBM - 1) / umma::kBM);
+}
+
+DraftWs carve_draft(void* base, int B, int K) {
   DraftWs w;
   size_t off = 0;
   auto take = [&](size_t n) {
@@ -380,11 +391,13 @@ DraftWs carve_draft(void* base, int B) {
     off = align_up(off + n, 256);
     return o;
   };
-  size_t o_part = take((size_t)kMaxGemvCtas * B * sizeof(float2));
+  size_t o_part = take((size_t)max_groups(K) * B * sizeof(float2));
   size_t o_z = take((size_t)B * kMaxFinChunks * sizeof(float));
   size_t o_l = take((size_t)B * kMaxFinChunks * sizeof(int));
   size_t o_c = take((size_t)B * sizeof(int));
+  size_t o_s = take(sizeof(int));
   char* p = static_cast<char*>(base);
+  w.status_sink = reinterpret_cast<int*>(p + o_s);
   w.part = reinterpret_cast<float2*>(p + o_part);
   w.zpart = reinterpret_cast<float*>(p + o_z);
   w.lpart = reinterpret_cast<int*>(p + o_l);
@@ -441,6 +454,100 @@ int launch_gemv(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   return e == cudaSuccess ? VT_OK : VT_ERR_CUDA;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D tensor map of a row-major bf16 [rows, cols] matrix, boxes of
+// 64 columns (128 bytes, 128-byte swizzle) x box_rows rows
+bool make_bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
+  auto fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool umma_supported(const uint16_t* hidden, int B, int H, const uint16_t* W) {
+  return B <= 256 && H % 8 == 0 && ((reinterpret_cast<uintptr_t>(hidden) & 15) == 0) &&
+         ((reinterpret_cast<uintptr_t>(W) & 15) == 0) && tensor_map_encoder() != nullptr;
+}
+
+template <int BN>
+int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
+                   umma::HeadArgs a, int tiles) {
+  constexpr int stage = umma::kABytes + BN * 128;
+  // up to ~110 KB of stages for narrow batches (two CTAs per SM), ~200 KB
+  // for wide ones (one CTA per SM)
+  const int budget = (BN <= 64) ? 110 * 1024 : 200 * 1024;
+  a.stages = std::max(2, std::min(umma::kMaxStages, budget / stage));
+  const size_t smem = (size_t)a.stages * stage + 1024;
+  auto k = umma::head_umma_kernel<BN>;
+  VT_RETURN_IF_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  k<<<tiles, umma::kThreads, smem, s>>>(mw, mh, a);
+  VT_RETURN_IF_LAUNCH_FAILED();
+  return VT_OK;
+}
+
+// z = out_scale * hidden @ W^T on the tensor cores; part[tile][b] partials
+int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
+                float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
+                int* status, int status_reset, int* groups_out) {
+  const int BN = (B <= 16) ? 16 : (B <= 32) ? 32 : (B <= 64) ? 64 : (B <= 128) ? 128 : 256;
+  CUtensorMap mw, mh;
+  if (!make_bf16_map(&mw, W, (uint64_t)K, (uint64_t)H, umma::kBM)) return VT_ERR_CUDA;
+  if (!make_bf16_map(&mh, hidden, (uint64_t)B, (uint64_t)H, (uint32_t)BN)) return VT_ERR_CUDA;
+  umma::HeadArgs a;
+  a.B = B;
+  a.H = H;
+  a.K = K;
+  a.out_scale = out_scale;
+  a.out = out;
+  a.ldo = ldo;
+  a.part = part;
+  a.zero_ints = zero_ints;
+  a.nzero = nzero;
+  a.status = status;
+  a.status_reset = status_reset;
+  a.stages = 2;
+  const int tiles = (K + umma::kBM - 1) / umma::kBM;
+  *groups_out = tiles;
+  switch (BN) {
+    case 16: return launch_umma_bn<16>(s, mw, mh, a, tiles);
+    case 32: return launch_umma_bn<32>(s, mw, mh, a, tiles);
+    case 64: return launch_umma_bn<64>(s, mw, mh, a, tiles);
+    case 128: return launch_umma_bn<128>(s, mw, mh, a, tiles);
+    default: return launch_umma_bn<256>(s, mw, mh, a, tiles);
+  }
+}
+
+// the projection through whichever engine the shapes allow
+int launch_head(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
+                float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
+                int* status, int status_reset, int* groups_out) {
+  if (umma_supported(hidden, B, H, W))
+    return launch_umma(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status,
+                       status_reset, groups_out);
+  return launch_gemv(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
+                     status_reset ? status : nullptr, groups_out);
+}
+
 int check_draft_args(const uint16_t* hidden, int B, int H, const uint16_t* W_trim, int K,
                      float T) {
   if (!hidden || !W_trim) return VT_ERR_INVALID_ARG;
@@ -454,9 +561,8 @@ int check_draft_args(const uint16_t* hidden, int B, int H, const uint16_t* W_tri
 
 extern "C" size_t vt_draft_workspace_bytes(int32_t B, int32_t H, int32_t K) {
   (void)H;
-  (void)K;
-  if (B < 1) return 0;
-  return vt::carve_draft(nullptr, B).bytes;
+  if (B < 1 || K < 1) return 0;
+  return vt::carve_draft(nullptr, B, K).bytes;
 }
 
 extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
@@ -467,11 +573,13 @@ extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
   int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
   if (st != VT_OK) return st;
   if (!logits || ld_logits < K) return VT_ERR_INVALID_ARG;
-  (void)workspace;
-  (void)workspace_bytes;
-  int grid = 0;
-  return launch_gemv(static_cast<cudaStream_t>(stream), hidden, B, H, W_trim, K,
-                     1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, nullptr, &grid);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
+  DraftWs ws = carve_draft(workspace, B, K);
+  if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
+  int groups = 0;
+  return launch_head(static_cast<cudaStream_t>(stream), hidden, B, H, W_trim, K,
+                     1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, ws.status_sink, 1,
+                     &groups);
 }
 
 extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
@@ -485,13 +593,15 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   if (!trim_ids || !uniforms || !q || ldq < K || !tokens || ld_tokens < 1 || !dev_status)
     return VT_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
-  DraftWs ws = carve_draft(workspace, B);
+  DraftWs ws = carve_draft(workspace, B, K);
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  // the projection zeroes the finalize tickets and the status word (its first
+  // CTA runs before the finalize grid starts: same stream)
   int grid = 0;
-  st = launch_gemv(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part,
-                   ws.counters, B, dev_status, &grid);
+  st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part,
+                   ws.counters, B, dev_status, 1, &grid);
   if (st != VT_OK) return st;
 
   FinArgs fa;
