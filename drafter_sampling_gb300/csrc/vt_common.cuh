@@ -140,6 +140,16 @@ __device__ __forceinline__ int block_min_int(int v, int* smem) {
   return r;
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream
+// has completed and its writes are visible / let the next kernel launch.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) {
   return (x + a - 1) / a * a;
 }

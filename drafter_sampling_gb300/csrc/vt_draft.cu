@@ -34,8 +34,7 @@ namespace {
 
 constexpr int kGemvNT = 256;        // 8 warps
 constexpr int kRowsPerWarp = 8;     // 4 lanes per row
-constexpr int kMaxGemvCtas = 1024;
-constexpr int kMaxFinChunks = 64;
+constexpr int kGemvRowTile = 64;  // rows per CTA of the CUDA-core projection
 constexpr int kFinNT = 256;
 
 __device__ __forceinline__ void unpack_bf16x8(uint4 v, float* x) {
@@ -95,6 +94,7 @@ draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
     for (int b = 0; b < BT; ++b) { m[b] = kNegBig; s[b] = 0.f; }
 
     const int groups = (K + kRowsPerWarp - 1) / kRowsPerWarp;
+    // one group of 8 consecutive rows per warp: CTA g covers rows [64g, 64g+64)
     for (int g = blockIdx.x * (kGemvNT / 32) + warp; g < groups; g += gridDim.x * (kGemvNT / 32)) {
       const int row = g * kRowsPerWarp + rlane;
       float acc[BT];
@@ -200,162 +200,172 @@ struct FinArgs {
   float* q;          // in: z scaled to base 2; out: probabilities
   int64_t ldq;
   int B, K;
-  const float2* part;
+  const float2* part;  // [G][B] partials of consecutive row tiles
   int G;
+  int tile_rows;       // rows per partial (64 or 128; divides kFinChunk)
   const float* u;
   const int* trim_ids;
   int* tokens;
   int64_t ldt;
-  float* zpart;
-  int* lpart;
-  int nchunk;
-  int chunk_len;
-  int* counters;
   int* dev_status;
   int vec_ok;
 };
 
-// four consecutive values at j (multiple of 4); zeros past j1
-__device__ __forceinline__ void load4f(const float* p, int64_t j, int64_t j1, bool vec, float* x,
-                                       bool l2) {
-  if (vec && j + 3 < j1) {
-    float4 v = l2 ? __ldcg(reinterpret_cast<const float4*>(p + j))
-                  : *reinterpret_cast<const float4*>(p + j);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = (j + e < j1) ? (l2 ? __ldcg(p + j + e) : p[j + e]) : 0.f;
-  }
-}
+constexpr int kFinChunk = kFinNT * 4;  // ids normalised per CTA
 
+// Normalises q for one chunk of 1024 ids of row b and, in the CTA whose chunk
+// holds the sampled tile, draws the token.  The projection left one online-
+// softmax partial (m_t, s_t) per tile of consecutive rows; the tile masses
+// s_t 2^(m_t - m) in units of the global 2^m are therefore known to every CTA
+// without waiting on any other: all CTAs of row b scan the tile masses in
+// tile order to find the tile where the running mass passes u_b * S, and the
+// warp holding that tile scans its rows (ascending id) to pick the row.
 __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   __shared__ MS mred[kFinNT / 32];
   __shared__ float sred[kFinNT / 32];
   __shared__ int ired[kFinNT / 32];
-  __shared__ int s_last, s_cstar, s_pick;
-  __shared__ float s_target;
+  __shared__ int s_tile, s_last;
+  __shared__ float s_before;
   const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31;
   float* qrow = a.q + (int64_t)b * a.ldq;
-  const bool vec = a.vec_ok != 0;
+  griddep_wait();  // the projection has completed
 
-  // global (max, sum) of row b from the GEMV partials
-  MS v{kNegBig, 0.f};
-  for (int g = tid; g < a.G; g += kFinNT) {
-    float2 t = a.part[(int64_t)g * a.B + b];
-    v = ms_combine(v, MS{t.x, t.y});
+  // this thread's ids (four consecutive) and tiles (consecutive)
+  const int64_t j = (int64_t)c * kFinChunk + 4 * (int64_t)tid;
+  float z[4];
+  if (a.vec_ok && j + 3 < a.K) {
+    const float4 v = *reinterpret_cast<const float4*>(qrow + j);
+    z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) z[e] = (j + e < a.K) ? qrow[j + e] : kNegBig;
   }
-  v = block_ms_reduce<kFinNT>(v, mred);
-  if (!(v.s > 0.f && isfinite(v.s) && isfinite(v.m))) {
+  const int per = (a.G + kFinNT - 1) / kFinNT;
+  const int t0 = tid * per, t1 = min(a.G, t0 + per);
+  MS mine{kNegBig, 0.f};
+  for (int t = t0; t < t1; ++t) {
+    const float2 p = a.part[(int64_t)t * a.B + b];
+    mine = ms_combine(mine, MS{p.x, p.y});
+  }
+  const MS g = block_ms_reduce<kFinNT>(mine, mred);
+  if (!(g.s > 0.f && isfinite(g.s) && isfinite(g.m))) {
     if (c == 0 && tid == 0) {
       a.tokens[(int64_t)b * a.ldt] = -1;
       atomicOr(a.dev_status, VT_DEV_NONFINITE);
     }
     return;
   }
-  const float m = v.m, invS = 1.f / v.s;
+  const float m = g.m, invS = 1.f / g.s;
 
-  // normalise this chunk in place and sum it with the fixed-order tile scan
-  const int64_t j0 = (int64_t)c * a.chunk_len;
-  const int64_t j1 = min((int64_t)a.K, j0 + (int64_t)a.chunk_len);
-  float run = 0.f;
-  int lp = -1;
-  for (int64_t base = j0; base < j1; base += (int64_t)kFinNT * 4) {
-    const int64_t j = base + 4 * (int64_t)tid;
-    float x[4];
-    load4f(qrow, j, j1, vec, x, false);
+  // normalise this chunk in place
+  float w[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = (j + e < j1) ? exp2_approx(x[e] - m) * invS : 0.f;
-    if (vec && j + 3 < j1) {
-      *reinterpret_cast<float4*>(qrow + j) = make_float4(x[0], x[1], x[2], x[3]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (j + e < j1) qrow[j + e] = x[e];
-    }
+  for (int e = 0; e < 4; ++e) w[e] = (j + e < a.K) ? exp2_approx(z[e] - m) : 0.f;
+  if (a.vec_ok && j + 3 < a.K) {
+    *reinterpret_cast<float4*>(qrow + j) =
+        make_float4(w[0] * invS, w[1] * invS, w[2] * invS, w[3] * invS);
+  } else {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (x[e] > 0.f) lp = (int)(j + e);
-    const float t4 = ((x[0] + x[1]) + x[2]) + x[3];
-    float excl, tot;
-    block_scan_incl<kFinNT>(t4, sred, excl, tot);
-    run += tot;
+      if (j + e < a.K) qrow[j + e] = w[e] * invS;
   }
-  lp = block_max_int<kFinNT>(lp, ired);
-  if (tid == 0) {
-    a.zpart[(int64_t)b * a.nchunk + c] = run;
-    a.lpart[(int64_t)b * a.nchunk + c] = lp;
-    __threadfence();
-    s_last = (atomicAdd(a.counters + b, 1) == a.nchunk - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  griddep_launch_dependents();
 
+  // tile holding the draw: scan of tile masses in tile order
+  const float target = a.u[b] * g.s;
+  float mass = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const float2 p = a.part[(int64_t)t * a.B + b];
+    mass += p.y * exp2_approx(p.x - m);
+  }
+  float excl, tot;
+  const float incl = block_scan_incl<kFinNT>(mass, sred, excl, tot);
+  const int first = block_min_int<kFinNT>(incl > target ? tid : kFinNT, ired);
   if (tid == 0) {
-    const float* zp = a.zpart + (int64_t)b * a.nchunk;
-    float total = 0.f;
-    for (int k = 0; k < a.nchunk; ++k) total += __ldcg(zp + k);
-    const float target = a.u[b] * total;
-    float pre = 0.f;
-    int cstar = -1;
-    for (int k = 0; k < a.nchunk; ++k) {
-      const float zk = __ldcg(zp + k);
-      if (pre + zk > target) { cstar = k; break; }
-      pre += zk;
-    }
-    int glast = -1;
-    for (int k = 0; k < a.nchunk; ++k) glast = max(glast, __ldcg(a.lpart + (int64_t)b * a.nchunk + k));
-    s_cstar = cstar;
-    s_target = target - pre;
-    s_pick = glast;
+    s_tile = -1;
+    s_before = 0.f;
+    s_last = 0;
   }
   __syncthreads();
-  int pick = s_pick;
-  if (s_cstar >= 0) {
-    const int64_t c0 = (int64_t)s_cstar * a.chunk_len;
-    const int64_t c1 = min((int64_t)a.K, c0 + (int64_t)a.chunk_len);
-    const float target = s_target;
-    float run2 = 0.f;
-    int lp2 = -1;
-    __syncthreads();
-    if (tid == 0) s_pick = -1;
-    __syncthreads();
-    for (int64_t base = c0; base < c1; base += (int64_t)kFinNT * 4) {
-      const int64_t j = base + 4 * (int64_t)tid;
-      float x[4];
-      load4f(qrow, j, c1, vec, x, true);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (x[e] > 0.f) lp2 = (int)(j + e);
-      const float t4 = ((x[0] + x[1]) + x[2]) + x[3];
-      float excl, tot;
-      const float incl = block_scan_incl<kFinNT>(t4, sred, excl, tot);
-      const bool hit = (run2 + incl > target);
-      const int first = block_min_int<kFinNT>(hit ? tid : kFinNT, ired);
-      if (first < kFinNT) {
-        if (tid == first) {
-          float acc = run2 + excl;
-          int pk = -1, lastp = -1;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (x[e] > 0.f) lastp = (int)(j + e);
-            acc += x[e];
-            if (pk < 0 && acc > target) pk = (int)(j + e);
-          }
-          s_pick = (pk >= 0) ? pk : lastp;
-        }
-        __syncthreads();
+  if (tid == first) {
+    // walk this thread's tiles; if rounding hides the crossing, fall back to
+    // the last tile with mass in the range and its last weighted row
+    float run = excl;
+    int last_t = -1;
+    for (int t = t0; t < t1; ++t) {
+      const float2 p = a.part[(int64_t)t * a.B + b];
+      const float mt = p.y * exp2_approx(p.x - m);
+      if (mt > 0.f) last_t = t;
+      if (run + mt > target) {
+        s_tile = t;
+        s_before = run;
         break;
       }
-      run2 += tot;
+      run += mt;
     }
-    lp2 = block_max_int<kFinNT>(lp2, ired);
-    pick = (s_pick >= 0) ? s_pick : (lp2 >= 0 ? lp2 : pick);
+    if (s_tile < 0) {
+      s_tile = last_t;
+      s_last = 1;
+    }
   }
-  if (tid == 0) {
-    a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
-    a.counters[b] = 0;
+  __syncthreads();
+  int tsel = s_tile;
+  const float before = s_before;
+  bool force_last = s_last != 0;
+  if (first == kFinNT) {
+    // u * S at or above the summed masses (rounding): last tile with mass
+    tsel = -1;
+    for (int t = a.G - 1; t >= 0 && tsel < 0; --t)
+      if (a.part[(int64_t)t * a.B + b].y > 0.f) tsel = t;
+    force_last = true;
   }
+  if (tsel < 0) return;
+  const int64_t r0 = (int64_t)tsel * a.tile_rows;
+  if (r0 < (int64_t)c * kFinChunk || r0 >= (int64_t)(c + 1) * kFinChunk) return;
+
+  // this CTA holds the tile: its rows are consecutive threads of one warp
+  const int64_t r1 = min((int64_t)a.K, r0 + a.tile_rows);
+  const int owner_warp = (int)((r0 - (int64_t)c * kFinChunk) / 4) >> 5;
+  if ((tid >> 5) != owner_warp) return;
+  float v = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (j + e >= r0 && j + e < r1) v += w[e];
+  float x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  const float local = target - before;
+  const unsigned hit = force_last ? 0u : __ballot_sync(0xffffffffu, x > local);
+  int pick = -1;
+  if (hit) {
+    const int l = __ffs(hit) - 1;
+    if (lane == l) {
+      float acc = x - v;
+      int lastp = -1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (j + e < r0 || j + e >= r1) continue;
+        if (w[e] > 0.f) lastp = (int)(j + e);
+        acc += w[e];
+        if (pick < 0 && acc > local) pick = (int)(j + e);
+      }
+      if (pick < 0) pick = lastp;
+    }
+    pick = __shfl_sync(0xffffffffu, pick, l);
+  } else {
+    // last row with weight in the tile
+    int lp = -1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e >= r0 && j + e < r1 && w[e] > 0.f) lp = (int)(j + e);
+    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+    pick = lp;
+  }
+  if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
 }
 
 int num_sms() {
@@ -372,15 +382,13 @@ int num_sms() {
 
 struct DraftWs {
   float2* part;
-  float* zpart;
-  int* lpart;
-  int* counters;
   int* status_sink;  // status word of calls that report none (vt_draft_logits)
   size_t bytes;
 };
 
+// partial groups: one per 64-row tile (CUDA-core path) or 128-row tile
 int max_groups(int K) {
-  return std::max(kMaxGemvCtas, (K + umma::kBM - 1) / umma::kBM);
+  return (K + kGemvRowTile - 1) / kGemvRowTile;
 }
 
 DraftWs carve_draft(void* base, int B, int K) {
@@ -392,16 +400,10 @@ DraftWs carve_draft(void* base, int B, int K) {
     return o;
   };
   size_t o_part = take((size_t)max_groups(K) * B * sizeof(float2));
-  size_t o_z = take((size_t)B * kMaxFinChunks * sizeof(float));
-  size_t o_l = take((size_t)B * kMaxFinChunks * sizeof(int));
-  size_t o_c = take((size_t)B * sizeof(int));
   size_t o_s = take(sizeof(int));
   char* p = static_cast<char*>(base);
   w.status_sink = reinterpret_cast<int*>(p + o_s);
   w.part = reinterpret_cast<float2*>(p + o_part);
-  w.zpart = reinterpret_cast<float*>(p + o_z);
-  w.lpart = reinterpret_cast<int*>(p + o_l);
-  w.counters = reinterpret_cast<int*>(p + o_c);
   w.bytes = off;
   return w;
 }
@@ -439,9 +441,9 @@ int launch_gemv(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   // the hidden tile must fit in shared memory
   while (bt > 1 && (size_t)bt * H * 2 > 160 * 1024) bt >>= 1;
   if ((size_t)bt * H * 2 > 200 * 1024) return VT_ERR_UNSUPPORTED;
+  // one CTA per 64 consecutive rows, so each partial covers one row tile
   const int rows_per_cta = (kGemvNT / 32) * kRowsPerWarp;
-  int grid = (K + rows_per_cta - 1) / rows_per_cta;
-  grid = std::max(1, std::min(grid, std::min(kMaxGemvCtas, 2 * num_sms())));
+  const int grid = (K + rows_per_cta - 1) / rows_per_cta;
   *grid_out = grid;
   cudaError_t e;
   switch (bt) {
@@ -500,8 +502,17 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
   const size_t smem = (size_t)a.stages * stage + 1024;
   auto k = umma::head_umma_kernel<BN>;
   VT_RETURN_IF_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  k<<<tiles, umma::kThreads, smem, s>>>(mw, mh, a);
-  VT_RETURN_IF_LAUNCH_FAILED();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(umma::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, k, mw, mh, a));
   return VT_OK;
 }
 
@@ -540,10 +551,13 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
 // the projection through whichever engine the shapes allow
 int launch_head(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
-                int* status, int status_reset, int* groups_out) {
-  if (umma_supported(hidden, B, H, W))
+                int* status, int status_reset, int* groups_out, int* tile_rows_out) {
+  if (umma_supported(hidden, B, H, W)) {
+    *tile_rows_out = umma::kBM;
     return launch_umma(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status,
                        status_reset, groups_out);
+  }
+  *tile_rows_out = kGemvRowTile;
   return launch_gemv(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
                      status_reset ? status : nullptr, groups_out);
 }
@@ -576,10 +590,10 @@ extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   DraftWs ws = carve_draft(workspace, B, K);
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
-  int groups = 0;
+  int groups = 0, tile_rows = 0;
   return launch_head(static_cast<cudaStream_t>(stream), hidden, B, H, W_trim, K,
                      1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, ws.status_sink, 1,
-                     &groups);
+                     &groups, &tile_rows);
 }
 
 extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
@@ -597,11 +611,11 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // the projection zeroes the finalize tickets and the status word (its first
-  // CTA runs before the finalize grid starts: same stream)
-  int grid = 0;
-  st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part,
-                   ws.counters, B, dev_status, 1, &grid);
+  // the projection zeroes the status word (its first CTA runs before the
+  // finalize grid starts: same stream)
+  int grid = 0, tile_rows = 0;
+  st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part, nullptr, 0,
+                   dev_status, 1, &grid, &tile_rows);
   if (st != VT_OK) return st;
 
   FinArgs fa;
@@ -611,25 +625,23 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   fa.K = K;
   fa.part = ws.part;
   fa.G = grid;
+  fa.tile_rows = tile_rows;
   fa.u = uniforms;
   fa.trim_ids = trim_ids;
   fa.tokens = tokens;
   fa.ldt = ld_tokens;
-  fa.zpart = ws.zpart;
-  fa.lpart = ws.lpart;
-  int nchunk = (num_sms() * 4 + B - 1) / B;
-  nchunk = std::max(1, std::min(nchunk, kMaxFinChunks));
-  nchunk = std::min(nchunk, std::max(1, K / 1024));
-  int len = (K + nchunk - 1) / nchunk;
-  len = (len + 3) / 4 * 4;
-  nchunk = (K + len - 1) / len;
-  fa.nchunk = nchunk;
-  fa.chunk_len = len;
-  fa.counters = ws.counters;
   fa.dev_status = dev_status;
   fa.vec_ok = ((reinterpret_cast<uintptr_t>(q) & 15) == 0) && (ldq % 4 == 0);
-  dim3 g2((unsigned)B, (unsigned)nchunk);
-  draft_finalize_kernel<<<g2, kFinNT, 0, s>>>(fa);
-  VT_RETURN_IF_LAUNCH_FAILED();
+  const int nchunk = (K + kFinChunk - 1) / kFinChunk;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B, (unsigned)nchunk);
+  cfg.blockDim = dim3(kFinNT);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, draft_finalize_kernel, fa));
   return VT_OK;
 }

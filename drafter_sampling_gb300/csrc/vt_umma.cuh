@@ -205,13 +205,16 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_h);
   }
-  if (tile == 0) {
-    for (int i = tid; i < a.nzero; i += kThreads) a.zero_ints[i] = 0;
-    if (tid == 0 && a.status_reset) *a.status = 0;
-  }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, kCols);
     tmem_relinquish();
+  }
+  // everything above overlaps the previous kernel's tail; from here on this
+  // kernel reads what earlier kernels wrote and writes what they may read
+  griddep_wait();
+  if (tile == 0) {
+    for (int i = tid; i < a.nzero; i += kThreads) a.zero_ints[i] = 0;
+    if (tid == 0 && a.status_reset) *a.status = 0;
   }
   fence_before_sync();
   __syncthreads();
@@ -262,8 +265,9 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   }
   __syncwarp();
 
-  // epilogue: all four warps
+  // epilogue: all four warps; the next kernel may launch meanwhile
   const bool acc_ok = mbar_wait(&acc_bar, 0);
+  griddep_launch_dependents();
   fence_after_sync();
   const int row = warp * 32 + lane;
   const int j = m0 + row;

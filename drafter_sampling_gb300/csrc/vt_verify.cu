@@ -93,12 +93,6 @@ __device__ __forceinline__ void online_update(float& m, float& s, const float* x
   for (int k = 0; k < N; ++k) s += exp2_approx(t[k] - m);
 }
 
-__device__ __forceinline__ void griddep_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 struct VArgs {
   const void* logits;
