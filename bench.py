@@ -81,7 +81,7 @@ KERNELS_PER_CALL = {"calibrate": 17, "trim": 4, "draft": 2, "verify": 2}
 KERNEL_SOURCES = {
     "calibrate": ["drafter_sampling_gb300/csrc/vt_calib.cu"],
     "trim": ["drafter_sampling_gb300/csrc/vt_calib.cu"],
-    "draft": ["drafter_sampling_gb300/csrc/vt_draft.cu"],
+    "draft": ["drafter_sampling_gb300/csrc/vt_draft.cu", "drafter_sampling_gb300/csrc/vt_umma.cuh"],
     "verify": ["drafter_sampling_gb300/csrc/vt_verify.cu"],
 }
 
