@@ -10,13 +10,13 @@
 // Kernels:
 //  * hist:    the Zipf head of a token stream would serialise a plain atomic
 //             histogram on a few addresses (the most frequent id alone is
-//             ~13% of the stream).  A sample of the first 256K ids picks the
-//             hot ids (sample count >= sample/4096); the main pass keeps a
-//             bitmap and a small hash table of them in shared memory and
-//             counts hot ids in per-CTA shared counters, cold ids with
-//             global atomics; lanes holding the same id merge first
-//             (match.any).  The sample only decides where an id is counted,
-//             so the counts are exact whatever it picks.
+//             ~13% of the stream).  A sample of the first 128K ids picks the
+//             hot ids (sample count >= 2) and the most frequent one; the main
+//             pass (one CTA per SM) counts the most frequent id in registers,
+//             the other hot ids in shared counters found through a bitmap-
+//             and-rank table, and cold ids with global atomics.  The sample
+//             only decides where an id is counted, so the counts are exact
+//             whatever it picks.
 //  * radix:   stable LSD radix sort of (~count, id) by 8-bit digits: per-tile
 //             digit counts, one exclusive scan, stable scatter.  Stability
 //             makes equal counts keep ascending id order, which is the tie
@@ -26,76 +26,147 @@
 //             counts, then tile-local scans that write trim_ids and inv_map),
 //             row gather of W.
 #include <algorithm>
+#include <utility>
 
 #include "vt_common.cuh"
 
 namespace vt {
 namespace {
 
-constexpr int kHistNT = 256;
-constexpr int kSortNT = 256;
-constexpr int kSortItems = 2;
-constexpr int kSortTile = kSortNT * kSortItems;
-constexpr int kScanNT = 1024;
+constexpr int kMainNT = 1024;           // main pass: one CTA of 32 warps per SM
 constexpr int kHotMax = 8192;            // hot ids counted in shared memory
 constexpr int64_t kSample = 1 << 17;     // ids in the hot-id sample
 constexpr unsigned kSampleThr = 2;       // sample count that makes an id hot
-constexpr int kHotBitmapMaxV = 1 << 19;  // bitmap + prefix of hot ids fit in 96 KB
+constexpr int kHotBitmapMaxV = 1 << 19;  // lookup table + hot counters fit in 160 KB
 
-// sample histogram of the first `ns` ids (warp-aggregated global atomics)
-__global__ void __launch_bounds__(kHistNT)
+// Sample histogram of the first `ns` ids.  Each CTA merges its kSampleIds
+// ids in a small open-addressing table in shared memory first, so a frequent
+// id costs one global atomic per CTA, not one per warp.
+constexpr int kSampleNT = 1024;
+constexpr int kSampleIds = 2048;   // ids per CTA
+constexpr int kHashBits = 12;
+constexpr int kHashSlots = 1 << kHashBits;  // > kSampleIds: every insert finds a slot
+
+__global__ void __launch_bounds__(kSampleNT)
 hist_sample_kernel(const int* __restrict__ ids, int64_t ns, int V, unsigned* __restrict__ tmp) {
-  const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * kHistNT;
-  for (int64_t i0 = (int64_t)blockIdx.x * kHistNT + threadIdx.x - lane; i0 < ns; i0 += stride) {
-    const int64_t i = i0 + lane;
-    const int id = (i < ns) ? __ldg(ids + i) : -1;
-    const bool ok = (unsigned)id < (unsigned)V;
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
-    if (ok && lane == __ffs(peers) - 1) atomicAdd(tmp + id, (unsigned)__popc(peers));
+  __shared__ int hkey[kHashSlots];
+  __shared__ unsigned hval[kHashSlots];
+  for (int i = threadIdx.x; i < kHashSlots; i += kSampleNT) {
+    hkey[i] = -1;
+    hval[i] = 0u;
+  }
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kSampleIds;
+  for (int e = threadIdx.x; e < kSampleIds; e += kSampleNT) {
+    const int64_t i = base + e;
+    if (i >= ns) break;
+    const int id = __ldg(ids + i);
+    if ((unsigned)id >= (unsigned)V) continue;
+    unsigned h = ((unsigned)id * 2654435761u) >> (32 - kHashBits);
+    for (int probe = 0; probe < kHashSlots; ++probe) {
+      const int k = atomicCAS(&hkey[h], -1, id);
+      if (k == -1 || k == id) {
+        atomicAdd(&hval[h], 1u);
+        break;
+      }
+      h = (h + 1u) & (kHashSlots - 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kHashSlots; i += kSampleNT) {
+    const int id = hkey[i];
+    if (id >= 0) atomicAdd(tmp + id, hval[i]);
   }
 }
 
-// ids whose sample count reaches `thr` (at most kHotMax, any order)
-__global__ void hot_select_kernel(const unsigned* __restrict__ tmp, int V, unsigned thr,
-                                  int* __restrict__ hot_list, int* __restrict__ hot_n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < V && tmp[i] >= thr) {
-    const int slot = atomicAdd(hot_n, 1);
+// Ids whose sample count reaches `thr` (at most kHotMax kept, any order; one
+// slot reservation per CTA), and the most frequent sampled id (ties: the
+// smaller id) as the key (count << 32) | (0xffffffff - id).
+constexpr int kSelNT = 256;
+
+__global__ void __launch_bounds__(kSelNT)
+hot_select_kernel(const unsigned* __restrict__ tmp, int V, unsigned thr, int* __restrict__ hot_list,
+                  int* __restrict__ hot_n, unsigned long long* __restrict__ top_key) {
+  __shared__ int wcnt[kSelNT / 32];
+  __shared__ unsigned long long wkey[kSelNT / 32];
+  __shared__ int sbase;
+  const int i = blockIdx.x * kSelNT + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned c = (i < V) ? tmp[i] : 0u;
+  const bool hot = c >= thr;
+  const unsigned mask = __ballot_sync(0xffffffffu, hot);
+  unsigned long long key = hot ? ((unsigned long long)c << 32) | (0xffffffffu - (unsigned)i) : 0ull;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+    key = other > key ? other : key;
+  }
+  if (lane == 0) {
+    wcnt[warp] = __popc(mask);
+    wkey[warp] = key;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tot = 0;
+    unsigned long long km = 0ull;
+    for (int w = 0; w < kSelNT / 32; ++w) {
+      tot += wcnt[w];
+      km = wkey[w] > km ? wkey[w] : km;
+    }
+    sbase = tot ? atomicAdd(hot_n, tot) : 0;
+    if (km) atomicMax(top_key, km);
+  }
+  __syncthreads();
+  if (hot) {
+    int slot = sbase + __popc(mask & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) slot += wcnt[w];
     if (slot < kHotMax) hot_list[slot] = i;
   }
 }
 
-// Hot ids: a bitmap over [0, V) in shared memory, and their slot = the rank
-// of their bit (per-word prefix counts + popc), so the shared counters are
-// indexed without a search.  Hot ids take shared atomics (contention stays
-// inside one SM); the rest take global atomics, where no address is hot.
-__global__ void __launch_bounds__(kHistNT)
+// Main pass, one CTA per SM.  Hot ids are found through a lookup table in
+// shared memory, one 32-bit word per 16 ids: the low half is the bitmap of
+// the hot ids among 16w..16w+15, the high half the number of hot ids below
+// 16w, so an id's hot-counter slot is one 4-byte load and a popc away.  The
+// most frequent sampled id is counted in a register (it alone would put
+// several lanes of most warps on one shared counter); other hot ids take
+// shared atomics; cold ids, where no address is hot, global atomics.  Every
+// CTA adds its nonzero hot counters to `counts` at the end.
+constexpr int kLutIds = 16;  // ids per lookup word
+
+__device__ __forceinline__ int lut_slot(unsigned e, int id) {
+  const unsigned bit = 1u << (id & (kLutIds - 1));
+  return (e & bit) ? (int)(e >> 16) + __popc(e & (bit - 1u)) : -1;
+}
+
+template <bool HOT>
+__global__ void __launch_bounds__(kMainNT, 1)
 hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __restrict__ hot_list,
-                 const int* __restrict__ hot_n, unsigned* __restrict__ counts,
-                 int* __restrict__ dev_status, int vec_ok, int use_hot) {
-  extern __shared__ unsigned smem[];
-  const int nwords = (V + 31) / 32;
-  unsigned* bitmap = smem;                                              // [nwords]
-  unsigned short* prefix = reinterpret_cast<unsigned short*>(smem + nwords);  // [nwords]
-  unsigned* hcnt = smem + nwords + (nwords + 1) / 2;                    // [kHotMax]
-  __shared__ int wsum[kHistNT / 32];
+                 const int* __restrict__ hot_n, const unsigned long long* __restrict__ top_key,
+                 unsigned* __restrict__ counts, int* __restrict__ dev_status, int vec_ok) {
+  extern __shared__ unsigned lut[];  // [nwords]
+  const int nwords = (V + kLutIds - 1) / kLutIds;
+  unsigned* hcnt = lut + nwords;     // [kHotMax]
+  __shared__ int wsum[kMainNT / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (use_hot) {
-    for (int w = tid; w < nwords; w += kHistNT) bitmap[w] = 0;
-    for (int h = tid; h < kHotMax; h += kHistNT) hcnt[h] = 0;
+  int top = -1;
+  if (HOT) {
+    for (int w = tid; w < nwords; w += kMainNT) lut[w] = 0u;
+    for (int h = tid; h < kHotMax; h += kMainNT) hcnt[h] = 0u;
+    const unsigned long long tk = *top_key;
+    if (tk != 0ull) top = (int)(0xffffffffu - (unsigned)(tk & 0xffffffffull));
     __syncthreads();
     const int nh = min(*hot_n, kHotMax);
-    for (int sl = tid; sl < nh; sl += kHistNT) {
+    for (int sl = tid; sl < nh; sl += kMainNT) {
       const int id = hot_list[sl];
-      atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+      atomicOr(&lut[id / kLutIds], 1u << (id & (kLutIds - 1)));
     }
     __syncthreads();
-    // prefix[w] = number of hot ids in words before w
-    const int per = (nwords + kHistNT - 1) / kHistNT;
+    // high half of lut[w] = number of hot ids in the words before w (< 2^13)
+    const int per = (nwords + kMainNT - 1) / kMainNT;
     const int w0 = tid * per, w1 = min(nwords, w0 + per);
     int c = 0;
-    for (int w = w0; w < w1; ++w) c += __popc(bitmap[w]);
+    for (int w = w0; w < w1; ++w) c += __popc(lut[w]);
     int x = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -107,202 +178,359 @@ hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __res
     int run = x - c;
     for (int w = 0; w < warp; ++w) run += wsum[w];
     for (int w = w0; w < w1; ++w) {
-      prefix[w] = (unsigned short)run;
-      run += __popc(bitmap[w]);
+      const unsigned bits = lut[w];
+      lut[w] = bits | ((unsigned)run << 16);
+      run += __popc(bits);
     }
     __syncthreads();
   }
   int bad = 0;
-  auto count = [&](int id) {
-    if ((unsigned)id >= (unsigned)V) {
-      bad = 1;
-      return;
-    }
-    if (use_hot) {
-      const unsigned word = bitmap[id >> 5];
-      const unsigned bit = 1u << (id & 31);
-      if (word & bit) {
-        atomicAdd(&hcnt[prefix[id >> 5] + __popc(word & (bit - 1))], 1u);
-        return;
-      }
-    }
-    atomicAdd(counts + id, 1u);
+  unsigned ctop = 0;
+  // one id, without branches: in range or not, the top id, hot, cold
+  auto count1 = [&](int id, unsigned e) {
+    const bool inr = (unsigned)id < (unsigned)V;
+    const bool istop = HOT && id == top;
+    bad |= inr ? 0 : 1;
+    ctop += (inr && istop) ? 1u : 0u;
+    const int slot = HOT ? lut_slot(e, id) : -1;
+    if (inr && !istop && slot >= 0) atomicAdd(&hcnt[slot], 1u);
+    if (inr && !istop && slot < 0) atomicAdd(counts + id, 1u);
   };
-  const int64_t stride = (int64_t)gridDim.x * kHistNT;
-  const int64_t t0 = (int64_t)blockIdx.x * kHistNT + tid;
+  auto lookup = [&](int id) -> unsigned {
+    return (HOT && (unsigned)id < (unsigned)V) ? lut[id / kLutIds] : 0u;
+  };
+  // eight ids: all table loads first, then the counter updates
+  auto count8 = [&](const int* v) {
+    unsigned e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[k] = lookup(v[k]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) count1(v[k], e[k]);
+  };
+  const int64_t stride = (int64_t)gridDim.x * kMainNT;
+  const int64_t t0 = (int64_t)blockIdx.x * kMainNT + tid;
   int64_t tail_start = 0;
   if (vec_ok) {
     const int64_t nv = n / 4;
     const int4* v4 = reinterpret_cast<const int4*>(ids);
     int64_t i = t0;
-    for (; i + stride < nv; i += 2 * stride) {
-      const int4 a = __ldg(v4 + i), b = __ldg(v4 + i + stride);
-      count(a.x); count(a.y); count(a.z); count(a.w);
-      count(b.x); count(b.y); count(b.z); count(b.w);
+    for (; i + 3 * stride < nv; i += 4 * stride) {
+      int4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = __ldg(v4 + i + u * stride);
+      const int a0[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
+      count8(a0);
+      const int a1[8] = {q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+      count8(a1);
     }
-    if (i < nv) {
-      const int4 a = __ldg(v4 + i);
-      count(a.x); count(a.y); count(a.z); count(a.w);
+    for (; i < nv; i += stride) {
+      const int4 q = __ldg(v4 + i);
+      count1(q.x, lookup(q.x));
+      count1(q.y, lookup(q.y));
+      count1(q.z, lookup(q.z));
+      count1(q.w, lookup(q.w));
     }
     tail_start = nv * 4;
   }
-  for (int64_t i = tail_start + t0; i < n; i += stride) count(__ldg(ids + i));
+  for (int64_t i = tail_start + t0; i < n; i += stride) {
+    const int id = __ldg(ids + i);
+    count1(id, lookup(id));
+  }
   if (bad) atomicOr(dev_status, VT_DEV_BAD_ID);
-  if (use_hot) {
+  if (HOT) {
+    // the register counter of the top id: warp sums, one atomic per warp
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ctop += __shfl_xor_sync(0xffffffffu, ctop, o);
+    if (lane == 0 && ctop != 0u) atomicAdd(counts + top, ctop);
     __syncthreads();
-    // flush: each set bit of the bitmap is one hot id with its slot
-    for (int w = tid; w < nwords; w += kHistNT) {
-      unsigned word = bitmap[w];
-      int slot = prefix[w];
-      while (word) {
-        const int b = __ffs(word) - 1;
-        word &= word - 1;
+    // flush: each set bit of the table is one hot id with its slot
+    for (int w = tid; w < nwords; w += kMainNT) {
+      const unsigned e = lut[w];
+      unsigned bits = e & 0xffffu;
+      int slot = (int)(e >> 16);
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
         const unsigned c = hcnt[slot++];
-        if (c) atomicAdd(counts + w * 32 + b, c);
+        if (c) atomicAdd(counts + w * kLutIds + b, c);
       }
     }
   }
 }
 
 // ----------------------------------------------------------- radix sort
-__global__ void sort_init_kernel(const unsigned* __restrict__ counts, int V,
-                                 unsigned* __restrict__ keys, int* __restrict__ vals) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < V) {
-    keys[i] = ~counts[i];  // ascending ~count = descending count
-    vals[i] = i;
-  }
+// Stable LSD radix sort of the keys ~c[t] (ascending ~count = descending
+// count; equal counts keep ascending id order), values t.  Counts are at most
+// n, so only the low `bits` = bit length of n bits of ~count vary: they are
+// sorted in P passes of D <= 10 bits (P * D >= bits).  One launch per pass:
+// tiles of 4096 keys take a ticket in launch order; each ranks its keys by
+// digit (per-warp ballots and counters: within a tile keys keep index order),
+// publishes its digit counts, then adds up the counts of the tiles with
+// smaller tickets (which are running or done, so every wait ends), reorders
+// its keys by digit in shared memory and writes each digit's run to its
+// place.  The global digit counts of every pass come from one pass over the
+// counts beforehand.
+constexpr int kRsNT = 1024;
+constexpr int kRsItems = 4;                  // keys per thread
+constexpr int kRsTile = kRsNT * kRsItems;    // keys per tile
+constexpr int kRsWarps = kRsNT / 32;
+constexpr int kRsMaxD = 10;                  // digit bits: radix <= 1024
+constexpr int kRsMaxPasses = 4;
+constexpr int kRsMaxV = 1 << 22;
+constexpr uint32_t kRsSpinLimit = 1u << 22;
+
+struct SortPlan {
+  int passes, D, radix, ntiles;
+};
+
+SortPlan sort_plan(int64_t n, int V) {
+  const unsigned long long cmax = (unsigned long long)std::min<int64_t>(n, 0xffffffffll);
+  int bits = 1;
+  while (bits < 32 && (cmax >> bits) != 0ull) ++bits;
+  SortPlan p;
+  p.passes = (bits + kRsMaxD - 1) / kRsMaxD;
+  p.D = (bits + p.passes - 1) / p.passes;
+  p.radix = 1 << p.D;
+  p.ntiles = (V + kRsTile - 1) / kRsTile;
+  return p;
 }
 
-__global__ void __launch_bounds__(kSortNT)
-sort_count_kernel(const unsigned* __restrict__ keys, int V, int shift, int ntiles,
-                  int* __restrict__ ghist) {
-  __shared__ int h[256];
-  h[threadIdx.x] = 0;
-  __syncthreads();
-  const int64_t base = (int64_t)blockIdx.x * kSortTile;
+__device__ __forceinline__ unsigned rs_digit(unsigned key, int shift, int radix) {
+  return (key >> shift) & (unsigned)(radix - 1);
+}
+
+// global digit counts of every pass: ghist[p * radix + d]
+__global__ void __launch_bounds__(kRsNT)
+sort_hist_kernel(const unsigned* __restrict__ counts, int V, int passes, int D,
+                 unsigned* __restrict__ ghist) {
+  __shared__ unsigned sh[kRsMaxPasses << kRsMaxD];
+  griddep_wait();  // the counts are complete
+  const int radix = 1 << D;
+  for (int i = threadIdx.x; i < (passes << D); i += kRsNT) sh[i] = 0u;
+  const int64_t base = (int64_t)blockIdx.x * kRsTile;
+  const int lane = threadIdx.x & 31;
+  unsigned key[kRsItems];
+  bool valid[kRsItems];
 #pragma unroll
-  for (int it = 0; it < kSortItems; ++it) {
-    const int64_t i = base + it * kSortNT + threadIdx.x;
-    if (i < V) atomicAdd(&h[(keys[i] >> shift) & 255u], 1);
+  for (int r = 0; r < kRsItems; ++r) {
+    const int64_t i = base + r * kRsNT + threadIdx.x;
+    valid[r] = i < V;
+    key[r] = valid[r] ? ~counts[i] : 0u;
   }
   __syncthreads();
-  ghist[threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
+  // most counts are small, so most keys share their high digits: a warp
+  // whose keys all have the same digit adds once
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid[r]);
+    for (int p = 0; p < passes; ++p) {
+      const unsigned d = rs_digit(key[r], p * D, radix);
+      const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
+      if (__all_sync(0xffffffffu, d == d0 || !valid[r])) {
+        if (lane == 0 && vmask) atomicAdd(&sh[p * radix + d0], (unsigned)__popc(vmask));
+      } else if (valid[r]) {
+        atomicAdd(&sh[p * radix + d], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < (passes << D); i += kRsNT)
+    if (sh[i]) atomicAdd(ghist + i, sh[i]);
 }
 
-// exclusive scan of ghist in blocks of kScanBlock entries: each block scans
-// its entries in place (block-local offsets) and writes its total; the
-// scatter kernel adds the totals of the blocks before.
-constexpr int kScanBlock = kScanNT * 4;
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
-__global__ void __launch_bounds__(kScanNT)
-scan_blocks_kernel(int* __restrict__ a, int n, int* __restrict__ btot) {
-  __shared__ int wsum[kScanNT / 32];
+// exclusive scan of one value per thread over the block (kRsNT threads)
+__device__ __forceinline__ unsigned rs_block_excl(unsigned v, unsigned* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t j = (int64_t)blockIdx.x * kScanBlock + 4 * threadIdx.x;
-  int v[4], c = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    v[e] = (j + e < n) ? a[j + e] : 0;
-    c += v[e];
-  }
-  int x = c;
+  unsigned x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
-  int run = x - c, tot = 0;
-  for (int w = 0; w < kScanNT / 32; ++w) {
-    if (w < warp) run += wsum[w];
-    tot += wsum[w];
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (j + e < n) a[j + e] = run;
-    run += v[e];
-  }
-  if (threadIdx.x == 0) btot[blockIdx.x] = tot;
+  unsigned pre = 0u;
+  for (int w = 0; w < warp; ++w) pre += wsum[w];
+  __syncthreads();
+  return pre + x - v;
 }
 
-__global__ void __launch_bounds__(kSortNT)
-sort_scatter_kernel(const unsigned* __restrict__ keys_in, const int* __restrict__ vals_in, int V,
-                    int shift, int ntiles, const int* __restrict__ goff,
-                    const int* __restrict__ btot, int nblk,
-                    unsigned* __restrict__ keys_out, int* __restrict__ vals_out) {
-  __shared__ int base_d[256];
-  __shared__ int cnt_d[256];
-  __shared__ int wc[kSortNT / 32][256];
-  __shared__ int bpre[64];
+struct SortPassArgs {
+  const unsigned* counts;   // pass 0 reads keys ~counts[i] and values i
+  const unsigned* keys_in;
+  const int* vals_in;
+  unsigned* keys_out;       // not written by the last pass
+  int* vals_out;
+  int* topk_ids;            // written by the last pass: ranks < K
+  int K;
+  int V;
+  int shift;
+  int first, last;
+  const unsigned* ghist;    // [radix] global digit counts of this pass
+  unsigned* status;         // [ntiles][radix] (1 << 31 | tile count) once published
+  int* ticket;
+  int* dev_status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kRsNT, 1) sort_pass_kernel(SortPassArgs a) {
+  constexpr int R = 1 << D;
+  extern __shared__ unsigned rs_smem[];
+  unsigned* whist = rs_smem;                // [kRsWarps][R]: warp counts, then warp offsets
+  unsigned* tstart = whist + kRsWarps * R;  // [R] first slot of digit d in the tile's order
+  unsigned* gpos = tstart + R;              // [R] global position of that slot
+  unsigned* skey = gpos + R;                // [kRsTile] keys in tile order
+  int* sval = reinterpret_cast<int*>(skey + kRsTile);
+  __shared__ int s_tile;
+  __shared__ unsigned wsum[kRsWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    int r = 0;
-    for (int k = 0; k < nblk; ++k) {
-      bpre[k] = r;
-      r += btot[k];
+  griddep_wait();  // the previous pass (or the counts) is complete
+  if (tid == 0) s_tile = atomicAdd(a.ticket, 1);
+  for (int i = tid; i < kRsWarps * R; i += kRsNT) whist[i] = 0u;
+  __syncthreads();
+  const int tile = s_tile;
+  const int64_t tbase = (int64_t)tile * kRsTile;
+  const int tcnt = (int)((int64_t)a.V - tbase < (int64_t)kRsTile ? (int64_t)a.V - tbase : (int64_t)kRsTile);
+
+  // load (warp-striped: item r of lane l is key 128 w + 32 r + l of the tile)
+  unsigned key[kRsItems];
+  int val[kRsItems];
+  unsigned rd[kRsItems];  // (rank within the warp << 11) | digit; digit == R: no key
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    const int j = warp * (32 * kRsItems) + 32 * r + lane;
+    const bool valid = j < tcnt;
+    const int64_t i = tbase + j;
+    if (a.first) {
+      key[r] = valid ? ~a.counts[i] : 0u;
+      val[r] = (int)i;
+    } else {
+      key[r] = valid ? a.keys_in[i] : 0u;
+      val[r] = valid ? a.vals_in[i] : 0;
     }
+    rd[r] = valid ? ((key[r] >> a.shift) & (unsigned)(R - 1)) : (unsigned)R;
+  }
+  // rank: lanes with the same digit found with one ballot per digit bit
+  unsigned* wh = whist + warp * R;
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    const unsigned d = rd[r];
+    const bool valid = d < (unsigned)R;
+    unsigned peers = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int b = 0; b < D; ++b) {
+      const unsigned m = __ballot_sync(0xffffffffu, (d >> b) & 1u);
+      peers &= ((d >> b) & 1u) ? m : ~m;
+    }
+    const unsigned before = valid ? wh[d] : 0u;
+    rd[r] = ((before + __popc(peers & lt)) << 11) | d;
+    __syncwarp();
+    if (valid && (peers & lt) == 0u) wh[d] = before + __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
-  {
-    const int e = tid * ntiles + blockIdx.x;
-    base_d[tid] = goff[e] + bpre[e / kScanBlock];
+
+  // per digit: warp offsets, the tile count (published), tile and global starts
+  unsigned tc = 0u;
+  if (tid < R) {
+    unsigned run = 0u;
+    for (int w = 0; w < kRsWarps; ++w) {
+      const unsigned c = whist[w * R + tid];
+      whist[w * R + tid] = run;
+      run += c;
+    }
+    tc = run;
+    st_relaxed_u32(a.status + (int64_t)tile * R + tid, 0x80000000u | tc);
   }
-  cnt_d[tid] = 0;
-  const int64_t base = (int64_t)blockIdx.x * kSortTile;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int it = 0; it < kSortItems; ++it) {
-    for (int k = tid; k < (kSortNT / 32) * 256; k += kSortNT) (&wc[0][0])[k] = 0;
-    __syncthreads();
-    const int64_t i = base + it * kSortNT + tid;
-    const bool valid = i < V;
-    unsigned key = 0;
-    int val = 0, d = 256;
-    if (valid) {
-      key = keys_in[i];
-      val = vals_in[i];
-      d = (key >> shift) & 255u;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    const int rank = __popc(peers & lt_mask);
-    if (valid && rank == 0) wc[warp][d] = __popc(peers);
-    __syncthreads();
-    if (valid) {
-      int pre = 0;
-      for (int w = 0; w < warp; ++w) pre += wc[w][d];
-      const int pos = base_d[d] + cnt_d[d] + pre + rank;
-      keys_out[pos] = key;
-      vals_out[pos] = val;
-    }
-    __syncthreads();
-    {
-      int tot = 0;
+  const unsigned ts = rs_block_excl(tc, wsum);
+  const unsigned gx = rs_block_excl(tid < R ? a.ghist[tid] : 0u, wsum);
+  if (tid < R) {
+    tstart[tid] = ts;
+    gpos[tid] = gx;
+  }
+  __syncthreads();
+  // counts of the tiles before this one: kRsNT / R threads per digit, each
+  // with up to 16 loads in flight (a count not yet published is polled)
+  bool timed_out = false;
+  {
+    constexpr int tpd = (kRsNT / R) > 0 ? (kRsNT / R) : 1;
+    const int d = tid % R, h = tid / R;
+    unsigned part = 0u;
+    for (int t0 = h; t0 < tile; t0 += 16 * tpd) {
+      unsigned v[16];
 #pragma unroll
-      for (int w = 0; w < kSortNT / 32; ++w) tot += wc[w][tid];
-      cnt_d[tid] += tot;
+      for (int j = 0; j < 16; ++j) {
+        const int t = t0 + j * tpd;
+        v[j] = (t < tile) ? ld_relaxed_u32(a.status + (int64_t)t * R + d) : 0x80000000u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = t0 + j * tpd;
+        const unsigned* sp = a.status + (int64_t)t * R + d;
+        for (uint32_t it = 0; (v[j] >> 31) == 0u && it < kRsSpinLimit; ++it) v[j] = ld_relaxed_u32(sp);
+        if ((v[j] >> 31) == 0u) timed_out = true;
+        part += v[j] & 0x7fffffffu;
+      }
     }
-    __syncthreads();
+    if (part != 0u) atomicAdd(&gpos[d], part);
+  }
+  if (timed_out) atomicOr(a.dev_status, VT_DEV_TIMEOUT);
+  // reorder the tile by digit in shared memory (stable)
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    const unsigned d = rd[r] & 2047u;
+    if (d >= (unsigned)R) continue;
+    const unsigned slot = tstart[d] + whist[warp * R + d] + (rd[r] >> 11);
+    skey[slot] = key[r];
+    sval[slot] = val[r];
+  }
+  __syncthreads();
+  // write out: consecutive slots of one digit go to consecutive positions
+  for (int j = tid; j < tcnt; j += kRsNT) {
+    const unsigned k = skey[j];
+    const unsigned d = (k >> a.shift) & (unsigned)(R - 1);
+    const unsigned pos = gpos[d] + ((unsigned)j - tstart[d]);
+    if (pos >= (unsigned)a.V) continue;  // only after a timed-out wait
+    if (a.last) {
+      if (pos < (unsigned)a.K) a.topk_ids[pos] = sval[j];
+    } else {
+      a.keys_out[pos] = k;
+      a.vals_out[pos] = sval[j];
+    }
   }
 }
 
-// zero the counts, the sample histogram, the hot-id count and the status
+template <int D>
+cudaError_t launch_sort_pass(const SortPassArgs& a, int ntiles, cudaStream_t s);
+
+// zero the counts, the sample histogram, the hot-id count, the top key, the
+// status word and the sort's tickets, digit counts and tile counts
 __global__ void calib_zero_kernel(unsigned* __restrict__ counts, unsigned* __restrict__ tmp, int V,
-                                  int* __restrict__ hot_n, int* __restrict__ dev_status) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < V) {
-    counts[i] = 0;
-    tmp[i] = 0;
+                                  int* __restrict__ hot_n, unsigned long long* __restrict__ top_key,
+                                  int* __restrict__ dev_status, unsigned* __restrict__ zero_words,
+                                  int64_t nzero) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = t0; i < V; i += stride) {
+    counts[i] = 0u;
+    tmp[i] = 0u;
   }
-  if (i == 0) {
+  for (int64_t i = t0; i < nzero; i += stride) zero_words[i] = 0u;
+  if (t0 == 0) {
     *hot_n = 0;
+    *top_key = 0ull;
     *dev_status = 0;
   }
-}
-
-__global__ void copy_ints_kernel(const int* __restrict__ src, int* __restrict__ dst, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) dst[i] = src[i];
 }
 
 // ------------------------------------------------------------------ trim
@@ -435,15 +663,21 @@ trim_gather_kernel(const uint16_t* __restrict__ W, int H, const int* __restrict_
 struct CalibWs {
   unsigned* keys[2];
   int* vals[2];
-  int* ghist;
-  int* btot;       // [64] block totals of the offset scan
   unsigned* tmp;   // sample histogram [V]
   int* hot_list;   // [kHotMax]
   int* hot_n;      // [1]
+  unsigned long long* top_key;  // [1] most frequent sampled id, packed with its count
+  // sort state, zeroed before each call (one contiguous block):
+  int* tickets;                 // [kRsMaxPasses]
+  unsigned* ghist;              // [passes][radix]
+  unsigned* status;             // [passes][ntiles][radix]
+  unsigned* zero_base;
   size_t bytes;
 };
 
-CalibWs carve_calib(void* base, int V) {
+// Workspace sized for the largest sort plan (4 passes, radix 1024); the
+// zeroed block is laid out for the plan actually used.
+CalibWs carve_calib(void* base, int V, const SortPlan* plan) {
   CalibWs w;
   size_t off = 0;
   auto take = [&](size_t n) {
@@ -451,26 +685,63 @@ CalibWs carve_calib(void* base, int V) {
     off = align_up(off + n, 256);
     return o;
   };
-  const int ntiles = (V + kSortTile - 1) / kSortTile;
+  const size_t ntiles = (size_t)(V + kRsTile - 1) / kRsTile;
   size_t k0 = take((size_t)V * 4), k1 = take((size_t)V * 4);
   size_t v0 = take((size_t)V * 4), v1 = take((size_t)V * 4);
-  size_t gh = take((size_t)256 * ntiles * 4);
-  size_t bt = take(64 * 4);
   size_t tm = take((size_t)V * 4);
   size_t hl = take((size_t)kHotMax * 4);
   size_t hn = take(4);
+  size_t tk = take(8);
+  const size_t zmax = 256 + (size_t)kRsMaxPasses * (1u << kRsMaxD) * 4 +
+                      (size_t)kRsMaxPasses * ntiles * (1u << kRsMaxD) * 4;
+  size_t zb = take(zmax);
   char* p = static_cast<char*>(base);
-  w.btot = reinterpret_cast<int*>(p + bt);
   w.tmp = reinterpret_cast<unsigned*>(p + tm);
   w.hot_list = reinterpret_cast<int*>(p + hl);
   w.hot_n = reinterpret_cast<int*>(p + hn);
+  w.top_key = reinterpret_cast<unsigned long long*>(p + tk);
   w.keys[0] = reinterpret_cast<unsigned*>(p + k0);
   w.keys[1] = reinterpret_cast<unsigned*>(p + k1);
   w.vals[0] = reinterpret_cast<int*>(p + v0);
   w.vals[1] = reinterpret_cast<int*>(p + v1);
-  w.ghist = reinterpret_cast<int*>(p + gh);
+  w.zero_base = reinterpret_cast<unsigned*>(p + zb);
+  w.tickets = reinterpret_cast<int*>(p + zb);
+  if (plan != nullptr) {
+    const size_t gh = (size_t)plan->passes * plan->radix * 4;
+    w.ghist = reinterpret_cast<unsigned*>(p + zb + 256);
+    w.status = reinterpret_cast<unsigned*>(p + zb + align_up(256 + gh, 256));
+  } else {
+    w.ghist = nullptr;
+    w.status = nullptr;
+  }
   w.bytes = off;
   return w;
+}
+
+// words of the zeroed block that `plan` uses
+int64_t calib_zero_words(int V, const SortPlan& plan) {
+  const size_t gh = (size_t)plan.passes * plan.radix * 4;
+  const size_t st = (size_t)plan.passes * plan.ntiles * plan.radix * 4;
+  (void)V;
+  return (int64_t)((align_up(256 + gh, 256) + st) / 4);
+}
+
+// launch with programmatic stream serialisation: the kernel may start while
+// the previous one drains and waits (griddepcontrol.wait) before reading
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 int num_sms() {
@@ -488,11 +759,25 @@ int num_sms() {
 }  // namespace
 }  // namespace vt
 
+namespace vt {
+namespace {
+template <int D>
+cudaError_t launch_sort_pass(const SortPassArgs& a, int ntiles, cudaStream_t s) {
+  constexpr int R = 1 << D;
+  const size_t smem = ((size_t)kRsWarps * R + 2 * R + 2 * (size_t)kRsTile) * 4;
+  cudaError_t e = cudaFuncSetAttribute(sort_pass_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(sort_pass_kernel<D>, dim3((unsigned)ntiles), dim3(kRsNT), smem, s, a);
+}
+}  // namespace
+}  // namespace vt
+
 extern "C" size_t vt_calibrate_topk_workspace_bytes(int64_t n, int32_t V, int32_t K) {
   (void)n;
   (void)K;
-  if (V < 1) return 0;
-  return vt::carve_calib(nullptr, V).bytes;
+  if (V < 1 || V > vt::kRsMaxV) return 0;
+  return vt::carve_calib(nullptr, V, nullptr).bytes;
 }
 
 extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
@@ -501,12 +786,18 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
   using namespace vt;
   if (n < 0 || V < 1 || V > (1 << 30) || K < 1 || K > V) return VT_ERR_INVALID_ARG;
   if ((n > 0 && !ids) || !counts || !topk_ids || !dev_status) return VT_ERR_INVALID_ARG;
+  if (V > kRsMaxV) return VT_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
-  CalibWs ws = carve_calib(workspace, V);
+  const SortPlan plan = sort_plan(n, V);
+  CalibWs ws = carve_calib(workspace, V, &plan);
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  calib_zero_kernel<<<(V + 255) / 256, 256, 0, s>>>(counts, ws.tmp, V, ws.hot_n, dev_status);
+  const int64_t nzero = calib_zero_words(V, plan);
+  const int64_t zwork = std::max<int64_t>(V, nzero);
+  const int zgrid = (int)std::min<int64_t>((zwork + 255) / 256, 4096);
+  calib_zero_kernel<<<zgrid, 256, 0, s>>>(counts, ws.tmp, V, ws.hot_n, ws.top_key, dev_status,
+                                          ws.zero_base, nzero);
   VT_RETURN_IF_LAUNCH_FAILED();
   if (n > 0) {
     const int vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
@@ -514,47 +805,66 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
     if (use_hot) {
       const int64_t ns = std::min<int64_t>(n, kSample);
       const unsigned thr = kSampleThr;
-      hist_sample_kernel<<<(unsigned)((ns + kHistNT - 1) / kHistNT), kHistNT, 0, s>>>(ids, ns, V,
-                                                                                   ws.tmp);
+      hist_sample_kernel<<<(unsigned)((ns + kSampleIds - 1) / kSampleIds), kSampleNT, 0, s>>>(
+          ids, ns, V, ws.tmp);
       VT_RETURN_IF_LAUNCH_FAILED();
-      hot_select_kernel<<<(V + 255) / 256, 256, 0, s>>>(ws.tmp, V, thr, ws.hot_list, ws.hot_n);
+      hot_select_kernel<<<(V + kSelNT - 1) / kSelNT, kSelNT, 0, s>>>(ws.tmp, V, thr, ws.hot_list,
+                                                                      ws.hot_n, ws.top_key);
       VT_RETURN_IF_LAUNCH_FAILED();
     }
-    const int nwords = (V + 31) / 32;
-    const size_t smem = use_hot ? ((size_t)nwords + (nwords + 1) / 2 + kHotMax) * 4 : 0;
-    if (smem > 48 * 1024)
-      VT_RETURN_IF_CUDA(cudaFuncSetAttribute(hist_main_kernel,
+    const int64_t want = (n / 4 + kMainNT - 1) / kMainNT;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms()));
+    if (use_hot) {
+      const size_t smem = ((size_t)(V + kLutIds - 1) / kLutIds + kHotMax) * 4;
+      VT_RETURN_IF_CUDA(cudaFuncSetAttribute(hist_main_kernel<true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem));
-    const int64_t want = (n / 4 + kHistNT - 1) / kHistNT;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
-    hist_main_kernel<<<grid, kHistNT, smem, s>>>(ids, n, V, ws.hot_list, ws.hot_n, counts,
-                                                 dev_status, vec_ok, use_hot);
+      hist_main_kernel<true><<<grid, kMainNT, smem, s>>>(ids, n, V, ws.hot_list, ws.hot_n,
+                                                         ws.top_key, counts, dev_status, vec_ok);
+    } else {
+      hist_main_kernel<false><<<grid, kMainNT, 0, s>>>(ids, n, V, ws.hot_list, ws.hot_n,
+                                                       ws.top_key, counts, dev_status, vec_ok);
+    }
     VT_RETURN_IF_LAUNCH_FAILED();
   }
-  sort_init_kernel<<<(V + 255) / 256, 256, 0, s>>>(counts, V, ws.keys[0], ws.vals[0]);
-  VT_RETURN_IF_LAUNCH_FAILED();
-  const int ntiles = (V + kSortTile - 1) / kSortTile;
-  const int nblk = (256 * ntiles + kScanBlock - 1) / kScanBlock;
-  if (nblk > 64) return VT_ERR_UNSUPPORTED;
-  int cur = 0;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 8 * pass;
-    sort_count_kernel<<<ntiles, kSortNT, 0, s>>>(ws.keys[cur], V, shift, ntiles, ws.ghist);
-    VT_RETURN_IF_LAUNCH_FAILED();
-    scan_blocks_kernel<<<nblk, kScanNT, 0, s>>>(ws.ghist, 256 * ntiles, ws.btot);
-    VT_RETURN_IF_LAUNCH_FAILED();
-    sort_scatter_kernel<<<ntiles, kSortNT, 0, s>>>(ws.keys[cur], ws.vals[cur], V, shift, ntiles,
-                                                   ws.ghist, ws.btot, nblk, ws.keys[cur ^ 1],
-                                                   ws.vals[cur ^ 1]);
-    VT_RETURN_IF_LAUNCH_FAILED();
-    cur ^= 1;
+
+  // Top-K: radix sort of (~count, id), one launch per pass
+  VT_RETURN_IF_CUDA(launch_pdl(sort_hist_kernel, dim3((unsigned)plan.ntiles), dim3(kRsNT), 0, s,
+                               (const unsigned*)counts, (int)V, plan.passes, plan.D, ws.ghist));
+  for (int p = 0; p < plan.passes; ++p) {
+    SortPassArgs a;
+    a.counts = counts;
+    a.keys_in = ws.keys[(p + 1) & 1];
+    a.vals_in = ws.vals[(p + 1) & 1];
+    a.keys_out = ws.keys[p & 1];
+    a.vals_out = ws.vals[p & 1];
+    a.topk_ids = topk_ids;
+    a.K = K;
+    a.V = V;
+    a.shift = p * plan.D;
+    a.first = p == 0;
+    a.last = p == plan.passes - 1;
+    a.ghist = ws.ghist + (size_t)p * plan.radix;
+    a.status = ws.status + (size_t)p * plan.ntiles * plan.radix;
+    a.ticket = ws.tickets + p;
+    a.dev_status = dev_status;
+    cudaError_t e;
+    switch (plan.D) {
+      case 1: e = launch_sort_pass<1>(a, plan.ntiles, s); break;
+      case 2: e = launch_sort_pass<2>(a, plan.ntiles, s); break;
+      case 3: e = launch_sort_pass<3>(a, plan.ntiles, s); break;
+      case 4: e = launch_sort_pass<4>(a, plan.ntiles, s); break;
+      case 5: e = launch_sort_pass<5>(a, plan.ntiles, s); break;
+      case 6: e = launch_sort_pass<6>(a, plan.ntiles, s); break;
+      case 7: e = launch_sort_pass<7>(a, plan.ntiles, s); break;
+      case 8: e = launch_sort_pass<8>(a, plan.ntiles, s); break;
+      case 9: e = launch_sort_pass<9>(a, plan.ntiles, s); break;
+      default: e = launch_sort_pass<10>(a, plan.ntiles, s); break;
+    }
+    VT_RETURN_IF_CUDA(e);
   }
-  copy_ints_kernel<<<(K + 255) / 256, 256, 0, s>>>(ws.vals[cur], topk_ids, K);
-  VT_RETURN_IF_LAUNCH_FAILED();
   return VT_OK;
 }
-
 extern "C" size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K) {
   (void)K;
   if (V < 1) return 0;

@@ -86,13 +86,16 @@ int vt_abi_version(void);
  *
  *  ids       int32 [n]       calibration token ids, each in [0, V)
  *  n         number of ids (>= 0)
- *  V         vocabulary size (1 <= V <= 2^30)
+ *  V         vocabulary size (1 <= V <= 2^30; V > 2^22 returns
+ *            VT_ERR_UNSUPPORTED in this build)
  *  K         number of ids kept (1 <= K <= V)
  *  counts    uint32 [V]      out: c[t] = occurrences of t (ids outside
  *                            [0, V) are skipped and flag VT_DEV_BAD_ID)
  *  topk_ids  int32 [K]       out: the K ids ranked by (count desc, id asc)
  *  dev_status int32 [1]      out: VT_DEV_* bits
  * Counts are exact (bit-identical to a sequential count) for n < 2^32.
+ * Workspace: vt_calibrate_topk_workspace_bytes(n, V, K) bytes, about
+ * 28 bytes per id of V (0 when V > 2^22).
  * ---------------------------------------------------------------------- */
 size_t vt_calibrate_topk_workspace_bytes(int64_t n, int32_t V, int32_t K);
 int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,

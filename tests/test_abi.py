@@ -52,6 +52,7 @@ def test_workspace_queries(lib):
     assert lib.vt_verify_workspace_bytes(0, 6, 10, 10) == 0
     assert lib.vt_draft_workspace_bytes(16, 2048, 32768) > 0
     assert lib.vt_calibrate_topk_workspace_bytes(1000, 128256, 32768) > 0
+    assert lib.vt_calibrate_topk_workspace_bytes(1000, (1 << 22) + 1, 10) == 0
 
 
 def test_host_argument_checks_need_no_gpu(lib):

@@ -37,6 +37,8 @@ def _calib(vt, ids, V, K):
     (1000, 50_000, 1, 0.5),         # K = 1
     (70_000, 1_000_001, 5000, 1.1),
     (17, 9, 5, 1.1),                # many zero counts (ties at 0)
+    (300_000, 2_100_000, 20_000, 1.1),  # counts need 22 bits: three sort passes, 37 tiles
+    (600_000, 1_000_003, 4096, 1.0),    # V beyond the shared-memory hot-id table
 ])
 def test_histogram_and_topk_bit_exact(vt, V, N, K, s):
     ids = synthetic.zipf_ids(N, V, s=s, seed=V + N)
@@ -58,6 +60,26 @@ def test_heavy_ties(vt):
         c, t, st = _calib(vt, ids, V, K)
         assert np.array_equal(c.astype(np.int64), target)
         assert np.array_equal(t, oracle.top_k(target, K))
+
+
+def test_heavy_ties_many_tiles(vt):
+    # 40000 ids over five sort tiles, counts in {0,..,5}: equal counts span tiles
+    g = synthetic.rng(91, 0)
+    V = 40_000
+    target = g.integers(0, 6, V)
+    ids = np.repeat(np.arange(V, dtype=np.int32), target)
+    ids = ids[g.permutation(ids.size)]
+    for K in [1, 8191, 8192, 8193, 39_999]:
+        c, t, st = _calib(vt, ids, V, K)
+        assert st == 0
+        assert np.array_equal(c.astype(np.int64), target)
+        assert np.array_equal(t, oracle.top_k(target, K))
+
+
+def test_vocabulary_above_sort_limit_is_unsupported(vt):
+    ids = torch.zeros(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(vt.VtError):
+        vt.vt_calibrate_topk(ids, (1 << 22) + 1, 10)
 
 
 def test_empty_stream(vt):

@@ -95,6 +95,8 @@ CASES = [
     (6, 3, 9000, 9000, "f32", 1.0, 0.0),     # q = p on the full vocabulary
     (8, 6, 20000, 3000, "f32", 1.0, 0.05),   # high acceptance: bonus draws
     (3, 64, 2048, 256, "bf16", 1.0, 0.3),    # the largest gamma
+    (2, 2, 262144, 5000, "f32", 1.0, 1.0),   # a large vocabulary: 128 residual tiles
+    (2, 3, 200003, 3000, "bf16", 0.9, 1.0),  # a large ragged vocabulary
 ]
 
 
