@@ -18,9 +18,13 @@
 //     stores z (scaled to base 2 for the softmax) and folds each CTA's rows
 //     into per-row-of-batch online-softmax partials (max, sum 2^(z - max)).
 //  2. draft_finalize grid (B, C): merges the partials, writes q = 2^(z-m)/S
-//     in place, and sums each chunk with a fixed-order tile scan; the last CTA
-//     of row b (atomic ticket, no waiting) finds the chunk where the running
-//     sum passes u_b * sum(q) and rescans it with the same tile scan.
+//     in place; every CTA scans the per-tile masses s_t 2^(m_t - m) in tile
+//     order (no CTA waits on another) to find the tile where the running
+//     mass passes u_b * S, and the CTA holding that tile scans its rows in
+//     ascending id order to pick the token.
+//  Both kernels are launched with programmatic dependent launch: the
+//  projection streams its first W_trim stages while the previous kernel in
+//  the stream drains.
 #include <algorithm>
 #include <cmath>
 
@@ -229,6 +233,9 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31;
   float* qrow = a.q + (int64_t)b * a.ldq;
+  // the next kernel may launch now: it reads nothing this kernel writes
+  // before its own griddepcontrol.wait, which waits for this whole grid
+  griddep_launch_dependents();
   griddep_wait();  // the projection has completed
 
   // this thread's ids (four consecutive) and tiles (consecutive)
@@ -270,7 +277,6 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     for (int e = 0; e < 4; ++e)
       if (j + e < a.K) qrow[j + e] = w[e] * invS;
   }
-  griddep_launch_dependents();
 
   // tile holding the draw: scan of tile masses in tile order
   const float target = a.u[b] * g.s;

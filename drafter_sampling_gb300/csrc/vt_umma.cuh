@@ -12,6 +12,10 @@
 // scale and store z and fold each tile's rows into per-batch-row online-
 // softmax partials (max, sum 2^(z - max)).
 //
+// The first ring stages of W_trim are requested before the kernel waits on
+// the previous kernel in the stream (programmatic dependent launch); the
+// hidden states and all outputs come after that wait.
+//
 // Every wait on an mbarrier is bounded: on expiry the kernel records
 // VT_DEV_TIMEOUT, drains its own TMA copies (bounded), frees its tensor memory
 // and returns.
@@ -209,23 +213,30 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     tmem_alloc(&tmem_base_sh, kCols);
     tmem_relinquish();
   }
-  // everything above overlaps the previous kernel's tail; from here on this
-  // kernel reads what earlier kernels wrote and writes what they may read
-  griddep_wait();
-  if (tile == 0) {
-    for (int i = tid; i < a.nzero; i += kThreads) a.zero_ints[i] = 0;
-    if (tid == 0 && a.status_reset) *a.status = 0;
-  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
+  // Everything above overlaps the previous kernel's tail.  The producer also
+  // fills the first stages with W_trim tiles before waiting on it: W_trim is
+  // a weight, never written by the kernel just before this one (the kernels
+  // of this library release their dependents only after their own wait, so
+  // every older kernel has completed).  Everything else -- the hidden states
+  // and every output -- waits for the previous kernel (griddepcontrol.wait).
   if (warp == 0 && lane == 0) {
     // TMA producer
-    int issued = 0;
+    const int pre = min(S, nk);
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_expect_tx(&full_bar[kb], (uint32_t)stage_bytes);
+      tma_load_2d(smem + (size_t)kb * stage_bytes, &map_w, kb * kBK, m0, &full_bar[kb]);
+    }
+    griddep_wait();
+    for (int kb = 0; kb < pre; ++kb)
+      tma_load_2d(smem + (size_t)kb * stage_bytes + kABytes, &map_h, kb * kBK, 0, &full_bar[kb]);
+    int issued = pre;
     bool ok = true;
-    for (int kb = 0; kb < nk && ok; ++kb) {
+    for (int kb = pre; kb < nk && ok; ++kb) {
       const int s = kb % S;
       if (kb >= S && !mbar_wait(&empty_bar[s], ((kb / S) - 1) & 1)) {
         ok = false;
@@ -241,7 +252,14 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     // drain: every issued copy has landed before this CTA may exit
     for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
       mbar_wait(&full_bar[kb % S], (kb / S) & 1);
-  } else if (warp == 1 && lane == 0) {
+  } else {
+    griddep_wait();
+    if (tile == 0 && warp >= 2) {
+      for (int i = tid - 64; i < a.nzero; i += kThreads - 64) a.zero_ints[i] = 0;
+      if (tid == 64 && a.status_reset) *a.status = 0;
+    }
+  }
+  if (warp == 1 && lane == 0) {
     // MMA issuer
     const uint32_t idesc = idesc_bf16_f32(kBM, BN);
     for (int kb = 0; kb < nk; ++kb) {
