@@ -26,9 +26,12 @@
 //             counts, then tile-local scans that write trim_ids and inv_map),
 //             row gather of W.
 #include <algorithm>
+#include <cooperative_groups.h>
 #include <utility>
 
 #include "vt_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vt {
 namespace {
@@ -127,34 +130,35 @@ hot_select_kernel(const unsigned* __restrict__ tmp, int V, unsigned thr, int* __
 // Main pass, one CTA per SM.  Hot ids are found through a lookup table in
 // shared memory, one 32-bit word per 16 ids: the low half is the bitmap of
 // the hot ids among 16w..16w+15, the high half the number of hot ids below
-// 16w, so an id's hot-counter slot is one 4-byte load and a popc away.  The
-// most frequent sampled id is counted in a register (it alone would put
-// several lanes of most warps on one shared counter); other hot ids take
-// shared atomics; cold ids, where no address is hot, global atomics.  Every
-// CTA adds its nonzero hot counters to `counts` at the end.
+// 16w, so an id's hot-counter slot is one 4-byte load and a popc away; a
+// zero word after the table answers every id >= V.  The most frequent
+// sampled id is counted in a register (it alone would put several lanes of
+// most warps on one shared counter); other hot ids take shared atomics; cold
+// ids, where no address is hot, global atomics.  Out-of-range ids are
+// detected once, from the largest id seen.  Every CTA adds its nonzero hot
+// counters to `counts` at the end.
 constexpr int kLutIds = 16;  // ids per lookup word
-
-__device__ __forceinline__ int lut_slot(unsigned e, int id) {
-  const unsigned bit = 1u << (id & (kLutIds - 1));
-  return (e & bit) ? (int)(e >> 16) + __popc(e & (bit - 1u)) : -1;
-}
 
 template <bool HOT>
 __global__ void __launch_bounds__(kMainNT, 1)
 hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __restrict__ hot_list,
                  const int* __restrict__ hot_n, const unsigned long long* __restrict__ top_key,
                  unsigned* __restrict__ counts, int* __restrict__ dev_status, int vec_ok) {
-  extern __shared__ unsigned lut[];  // [nwords]
+  extern __shared__ unsigned lut[];  // [nwords + 1]
   const int nwords = (V + kLutIds - 1) / kLutIds;
-  unsigned* hcnt = lut + nwords;     // [kHotMax]
+  unsigned* hcnt = lut + nwords + 1;  // [kHotMax]
   __shared__ int wsum[kMainNT / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int top = -1;
+  unsigned top = 0u;
+  bool use_top = false;  // a most frequent sampled id exists
   if (HOT) {
-    for (int w = tid; w < nwords; w += kMainNT) lut[w] = 0u;
+    for (int w = tid; w <= nwords; w += kMainNT) lut[w] = 0u;
     for (int h = tid; h < kHotMax; h += kMainNT) hcnt[h] = 0u;
     const unsigned long long tk = *top_key;
-    if (tk != 0ull) top = (int)(0xffffffffu - (unsigned)(tk & 0xffffffffull));
+    if (tk != 0ull) {
+      top = 0xffffffffu - (unsigned)(tk & 0xffffffffull);
+      use_top = top < (unsigned)V;
+    }
     __syncthreads();
     const int nh = min(*hot_n, kHotMax);
     for (int sl = tid; sl < nh; sl += kMainNT) {
@@ -184,23 +188,24 @@ hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __res
     }
     __syncthreads();
   }
-  int bad = 0;
-  unsigned ctop = 0;
-  // one id, without branches: in range or not, the top id, hot, cold
-  auto count1 = [&](int id, unsigned e) {
-    const bool inr = (unsigned)id < (unsigned)V;
-    const bool istop = HOT && id == top;
-    bad |= inr ? 0 : 1;
-    ctop += (inr && istop) ? 1u : 0u;
-    const int slot = HOT ? lut_slot(e, id) : -1;
-    if (inr && !istop && slot >= 0) atomicAdd(&hcnt[slot], 1u);
-    if (inr && !istop && slot < 0) atomicAdd(counts + id, 1u);
+  const unsigned uV = (unsigned)V, last = (unsigned)nwords;
+  unsigned umax = 0u;  // largest id seen (as unsigned: negative ids are huge)
+  unsigned ctop = 0u;
+  auto lookup = [&](unsigned uid) -> unsigned {
+    return HOT ? lut[min(uid / kLutIds, last)] : 0u;
   };
-  auto lookup = [&](int id) -> unsigned {
-    return (HOT && (unsigned)id < (unsigned)V) ? lut[id / kLutIds] : 0u;
+  auto count1 = [&](unsigned uid, unsigned e) {
+    umax = max(umax, uid);
+    const unsigned bit = 1u << (uid & (kLutIds - 1));
+    const bool is_top = HOT && use_top && uid == top;
+    const bool hot = !is_top && (e & bit) != 0u;
+    const bool cold = !is_top && (e & bit) == 0u && uid < uV;
+    ctop += is_top ? 1u : 0u;
+    if (hot) atomicAdd(&hcnt[(e >> 16) + __popc(e & (bit - 1u))], 1u);
+    if (cold) atomicAdd(counts + uid, 1u);
   };
   // eight ids: all table loads first, then the counter updates
-  auto count8 = [&](const int* v) {
+  auto count8 = [&](const unsigned* v) {
     unsigned e[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) e[k] = lookup(v[k]);
@@ -212,19 +217,19 @@ hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __res
   int64_t tail_start = 0;
   if (vec_ok) {
     const int64_t nv = n / 4;
-    const int4* v4 = reinterpret_cast<const int4*>(ids);
+    const uint4* v4 = reinterpret_cast<const uint4*>(ids);
     int64_t i = t0;
     for (; i + 3 * stride < nv; i += 4 * stride) {
-      int4 q[4];
+      uint4 q[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) q[u] = __ldg(v4 + i + u * stride);
-      const int a0[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
+      const unsigned a0[8] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w};
       count8(a0);
-      const int a1[8] = {q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+      const unsigned a1[8] = {q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
       count8(a1);
     }
     for (; i < nv; i += stride) {
-      const int4 q = __ldg(v4 + i);
+      const uint4 q = __ldg(v4 + i);
       count1(q.x, lookup(q.x));
       count1(q.y, lookup(q.y));
       count1(q.z, lookup(q.z));
@@ -233,15 +238,15 @@ hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __res
     tail_start = nv * 4;
   }
   for (int64_t i = tail_start + t0; i < n; i += stride) {
-    const int id = __ldg(ids + i);
-    count1(id, lookup(id));
+    const unsigned uid = (unsigned)__ldg(ids + i);
+    count1(uid, lookup(uid));
   }
-  if (bad) atomicOr(dev_status, VT_DEV_BAD_ID);
+  if (umax >= uV) atomicOr(dev_status, VT_DEV_BAD_ID);
   if (HOT) {
     // the register counter of the top id: warp sums, one atomic per warp
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ctop += __shfl_xor_sync(0xffffffffu, ctop, o);
-    if (lane == 0 && ctop != 0u) atomicAdd(counts + top, ctop);
+    if (lane == 0 && use_top && ctop != 0u) atomicAdd(counts + top, ctop);
     __syncthreads();
     // flush: each set bit of the table is one hot id with its slot
     for (int w = tid; w < nwords; w += kMainNT) {
@@ -630,11 +635,130 @@ trim_write_kernel(int* __restrict__ inv_map, int V, int K, const int* __restrict
     for (int p = s_all + threadIdx.x; p < K; p += kTrimNT) trim_ids[p] = -1;
 }
 
-// one warp per trimmed row: W_trim[j, :] = W[trim_ids[j], :]
+// Index mapper in one cluster of kIdxCL CTAs (V <= kIdxMaxV).  CTA r keeps
+// the bitmap of the kept ids among words [r * slice, (r + 1) * slice) in its
+// shared memory: every CTA reads all of topk_ids and marks the ids of its
+// slice (atomicOr's old value reports duplicates), scans its slice, learns
+// the kept-id counts of the other slices through distributed shared memory,
+// and writes, in ascending id order, its part of trim_ids and of a rank
+// table (bitmap word, kept ids before it) from which the gather kernel
+// writes inv_map.
+constexpr int kIdxNT = 1024;
+constexpr int kIdxCL = 8;
+constexpr int kIdxMaxV = 1 << 20;  // 16 KB of bitmap per CTA
+constexpr int kIdxBatch = 16;      // topk loads in flight per thread
+
+__global__ void __cluster_dims__(kIdxCL, 1, 1) __launch_bounds__(kIdxNT, 1)
+trim_index_kernel(const int* __restrict__ topk, int K, int V, int* __restrict__ trim_ids,
+                  uint2* __restrict__ table, int* __restrict__ dev_status) {
+  extern __shared__ unsigned bm[];  // [slice] bitmap words, then [slice] local prefix
+  __shared__ int wsum[kIdxNT / 32];
+  __shared__ int s_total;           // kept ids in this CTA's slice
+  __shared__ int s_tot[kIdxCL];     // kept ids in every slice
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwords = (V + 31) >> 5;
+  const int slice = (nwords + kIdxCL - 1) / kIdxCL;
+  unsigned* pre = bm + slice;
+  const int wbeg = rank * slice, wend = min(nwords, wbeg + slice);
+  griddep_wait();  // topk_ids come from the previous kernel
+  for (int w = tid; w < slice; w += kIdxNT) bm[w] = 0u;
+  if (rank == 0 && tid == 0) *dev_status = 0;
+  __syncthreads();
+  int flags = 0;
+  for (int k0 = tid; k0 < K; k0 += kIdxNT * kIdxBatch) {
+    int id[kIdxBatch];
+#pragma unroll
+    for (int r = 0; r < kIdxBatch; ++r) {
+      const int k = k0 + r * kIdxNT;
+      id[r] = (k < K) ? __ldg(topk + k) : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kIdxBatch; ++r) {
+      if (k0 + r * kIdxNT >= K) continue;  // past the end
+      if ((unsigned)id[r] >= (unsigned)V) {
+        flags |= VT_DEV_BAD_ID;
+        continue;
+      }
+      const int w = id[r] >> 5;
+      if (w < wbeg || w >= wend) continue;  // another CTA's slice
+      const unsigned bit = 1u << (id[r] & 31);
+      if (atomicOr(&bm[w - wbeg], bit) & bit) flags |= VT_DEV_DUPLICATE_ID;
+    }
+  }
+  if (flags && (rank == 0 || (flags & VT_DEV_DUPLICATE_ID))) atomicOr(dev_status, flags);
+  __syncthreads();
+
+  // local exclusive prefix of every word of the slice, in word order
+  int base = 0;
+  for (int r0 = wbeg; r0 < wend; r0 += kIdxNT) {
+    const int w = r0 + tid;
+    const int c = (w < wend) ? __popc(bm[w - wbeg]) : 0;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int run = base + x - c, rtot = 0;
+    for (int v = 0; v < kIdxNT / 32; ++v) {
+      if (v < warp) run += wsum[v];
+      rtot += wsum[v];
+    }
+    if (w < wend) pre[w - wbeg] = (unsigned)run;
+    __syncthreads();
+    base += rtot;
+  }
+  if (tid == 0) s_total = base;
+  cl.sync();
+  if (tid < kIdxCL) s_tot[tid] = *cl.map_shared_rank(&s_total, tid);
+  cl.sync();  // every remote read is done: CTAs may leave from here on
+  int before = 0, total = 0;
+  for (int q = 0; q < kIdxCL; ++q) {
+    if (q < rank) before += s_tot[q];
+    total += s_tot[q];
+  }
+  // table and trim_ids: a warp takes 32 consecutive words; for each of them
+  // lane l keeps id 32 w + l, so the word's kept ids land at consecutive
+  // positions (one coalesced store)
+  for (int r0 = wbeg; r0 < wend; r0 += kIdxNT) {
+    const int w = r0 + tid;
+    const unsigned bits = (w < wend) ? bm[w - wbeg] : 0u;
+    const int run = before + ((w < wend) ? (int)pre[w - wbeg] : 0);
+    if (w < wend) table[w] = make_uint2(bits, (unsigned)run);
+    for (int j = 0; j < 32; ++j) {
+      const unsigned wj = __shfl_sync(0xffffffffu, bits, j);
+      const int pj = __shfl_sync(0xffffffffu, run, j);
+      if ((wj >> lane) & 1u) {
+        const int pos = pj + __popc(wj & ((1u << lane) - 1u));
+        if (pos < K) trim_ids[pos] = (r0 + warp * 32 + j) * 32 + lane;
+      }
+    }
+  }
+  // fewer than K distinct ids (bad input): pad trim_ids
+  if (rank == kIdxCL - 1)
+    for (int p = total + tid; p < K; p += kIdxNT) trim_ids[p] = -1;
+}
+
+// one warp per trimmed row: W_trim[j, :] = W[trim_ids[j], :].  With a rank
+// table, thread g < V of the grid also writes inv_map[g].  This kernel
+// releases no dependent early: the projection kernel requests W_trim tiles
+// before its own dependency wait.
 __global__ void __launch_bounds__(256)
 trim_gather_kernel(const uint16_t* __restrict__ W, int H, const int* __restrict__ trim_ids, int K,
-                   int V, uint16_t* __restrict__ W_trim, int vec_ok) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+                   int V, uint16_t* __restrict__ W_trim, int vec_ok, const uint2* __restrict__ table,
+                   int* __restrict__ inv_map) {
+  griddep_wait();  // trim_ids (and the rank table) are complete
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (table != nullptr && g < V) {
+    const uint2 e = table[g >> 5];
+    const unsigned bit = 1u << (g & 31);
+    inv_map[g] = (e.x & bit) ? (int)(e.y + __popc(e.x & (bit - 1u))) : -1;
+  }
+  const int warp = (int)(g >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= K) return;
   const int id = trim_ids[warp];
@@ -815,7 +939,7 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
     const int64_t want = (n / 4 + kMainNT - 1) / kMainNT;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms()));
     if (use_hot) {
-      const size_t smem = ((size_t)(V + kLutIds - 1) / kLutIds + kHotMax) * 4;
+      const size_t smem = ((size_t)(V + kLutIds - 1) / kLutIds + 1 + kHotMax) * 4;
       VT_RETURN_IF_CUDA(cudaFuncSetAttribute(hist_main_kernel<true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem));
@@ -868,7 +992,10 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
 extern "C" size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K) {
   (void)K;
   if (V < 1) return 0;
-  return vt::align_up((size_t)((V + vt::kTrimTile - 1) / vt::kTrimTile) * 4, 256);
+  // rank table (8 bytes per 32 ids) when V <= kIdxMaxV, else tile counts
+  const size_t table = (size_t)((V + 31) / 32) * 8;
+  const size_t tiles = (size_t)((V + vt::kTrimTile - 1) / vt::kTrimTile) * 4;
+  return vt::align_up(std::max(table, tiles), 256);
 }
 
 extern "C" int vt_trim_head(const uint16_t* W, int32_t V, int32_t H, const int32_t* topk_ids,
@@ -881,6 +1008,21 @@ extern "C" int vt_trim_head(const uint16_t* W, int32_t V, int32_t H, const int32
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   if (workspace_bytes < vt_trim_head_workspace_bytes(V, K)) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int vec_ok = (H % 8 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(W_trim) & 15) == 0);
+  const int64_t gthreads = std::max<int64_t>((int64_t)K * 32, V);
+  const unsigned ggrid = (unsigned)((gthreads + 255) / 256);
+  if (V <= kIdxMaxV) {
+    // index mapper in one CTA, then the gather (which also writes inv_map)
+    uint2* table = static_cast<uint2*>(workspace);
+    const size_t smem = (size_t)(((V + 31) / 32 + kIdxCL - 1) / kIdxCL) * 8;
+    VT_RETURN_IF_CUDA(launch_pdl(trim_index_kernel, dim3(kIdxCL), dim3(kIdxNT), smem, s, topk_ids,
+                                 (int)K, (int)V, trim_ids, table, dev_status));
+    VT_RETURN_IF_CUDA(launch_pdl(trim_gather_kernel, dim3(ggrid), dim3(256), 0, s, W, (int)H,
+                                 (const int*)trim_ids, (int)K, (int)V, W_trim, vec_ok,
+                                 (const uint2*)table, inv_map));
+    return VT_OK;
+  }
   VT_RETURN_IF_CUDA(cudaMemsetAsync(inv_map, 0, (size_t)V * 4, s));
   VT_RETURN_IF_CUDA(cudaMemsetAsync(dev_status, 0, 4, s));
   trim_mark_kernel<<<(K + 255) / 256, 256, 0, s>>>(topk_ids, K, V, inv_map, dev_status);
@@ -891,11 +1033,7 @@ extern "C" int vt_trim_head(const uint16_t* W, int32_t V, int32_t H, const int32
   VT_RETURN_IF_LAUNCH_FAILED();
   trim_write_kernel<<<ntiles, kTrimNT, 0, s>>>(inv_map, V, K, tcount, ntiles, trim_ids);
   VT_RETURN_IF_LAUNCH_FAILED();
-  const int vec_ok = (H % 8 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(W_trim) & 15) == 0);
-  const int64_t warps = K;
-  trim_gather_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(W, H, trim_ids, K, V, W_trim,
-                                                                         vec_ok);
+  trim_gather_kernel<<<ggrid, 256, 0, s>>>(W, H, trim_ids, K, V, W_trim, vec_ok, nullptr, nullptr);
   VT_RETURN_IF_LAUNCH_FAILED();
   return VT_OK;
 }

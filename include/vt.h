@@ -113,7 +113,7 @@ int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
  *  trim_ids  int32 [K]       out: the selected ids, ascending (T_{d->t})
  *  inv_map   int32 [V]       out: inv_map[trim_ids[j]] = j, -1 elsewhere
  *  dev_status int32 [1]      out: VT_DEV_BAD_ID / VT_DEV_DUPLICATE_ID
- * Workspace: vt_trim_head_workspace_bytes(V, K) bytes (4 bytes per 1024 ids).
+ * Workspace: vt_trim_head_workspace_bytes(V, K) bytes (8 bytes per 32 ids).
  * ---------------------------------------------------------------------- */
 size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K);
 int vt_trim_head(const uint16_t* W, int32_t V, int32_t H,

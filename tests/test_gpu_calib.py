@@ -123,7 +123,9 @@ def test_calibration_full_size(vt):
         assert np.array_equal(t.cpu().numpy(), oracle.top_k(ref_c, K))
 
 
-@pytest.mark.parametrize("V,H,K", [(500, 24, 77), (1000, 13, 999), (64, 8, 64), (300, 3072, 1)])
+@pytest.mark.parametrize("V,H,K", [(500, 24, 77), (1000, 13, 999), (64, 8, 64), (300, 3072, 1),
+                                   (70_001, 16, 40_000),       # K above one index-kernel batch
+                                   ((1 << 20) + 37, 8, 5000)])  # V above the one-CTA index mapper
 def test_trim_head_bit_exact(vt, V, H, K):
     g = synthetic.rng(V + H + K, 0)
     W = g.integers(0, 65535, (V, H)).astype(np.uint16)
@@ -162,9 +164,17 @@ def test_trim_head_full_size(vt):
 
 def test_trim_head_flags_duplicates_and_range(vt):
     W = np.arange(40, dtype=np.uint16).reshape(10, 4)
-    _, _, _, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array([1, 3, 3], np.int32)))
+    Wt, ti, im, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array([1, 3, 3], np.int32)))
     torch.cuda.synchronize()
     assert int(st.item()) & vt.VT_DEV_DUPLICATE_ID
-    _, _, _, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array([1, 10], np.int32)))
-    torch.cuda.synchronize()
-    assert int(st.item()) & vt.VT_DEV_BAD_ID
+    # the distinct ids are kept in id order, the missing slot is -1
+    assert list(ti.cpu().numpy()) == [1, 3, -1]
+    expect = np.full(10, -1, np.int32)
+    expect[1], expect[3] = 0, 1
+    assert np.array_equal(im.cpu().numpy(), expect)
+    assert np.array_equal(Wt.cpu().numpy().view(np.uint16)[:2], W[[1, 3]])
+    for bad in ([1, 10], [-2, 4]):
+        _, ti, _, st = vt.vt_trim_head(_dev(W.view(np.int16)), _dev(np.array(bad, np.int32)))
+        torch.cuda.synchronize()
+        assert int(st.item()) & vt.VT_DEV_BAD_ID
+        assert sorted(ti.cpu().numpy().tolist()) == [-1, [b for b in bad if 0 <= b < 10][0]]
