@@ -197,6 +197,9 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   const int tile = blockIdx.x;
   const int m0 = tile * kBM;
   const int nk = (a.H + kBK - 1) / kBK;
+  // tiles start their reduction at different column blocks, so the rows
+  // streamed at any moment are spread over column offsets (DRAM channels)
+  const int rot = tile % nk;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -229,11 +232,13 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     const int pre = min(S, nk);
     for (int kb = 0; kb < pre; ++kb) {
       mbar_expect_tx(&full_bar[kb], (uint32_t)stage_bytes);
-      tma_load_2d(smem + (size_t)kb * stage_bytes, &map_w, kb * kBK, m0, &full_bar[kb]);
+      tma_load_2d(smem + (size_t)kb * stage_bytes, &map_w, ((kb + rot) % nk) * kBK, m0,
+                  &full_bar[kb]);
     }
     griddep_wait();
     for (int kb = 0; kb < pre; ++kb)
-      tma_load_2d(smem + (size_t)kb * stage_bytes + kABytes, &map_h, kb * kBK, 0, &full_bar[kb]);
+      tma_load_2d(smem + (size_t)kb * stage_bytes + kABytes, &map_h, ((kb + rot) % nk) * kBK, 0,
+                  &full_bar[kb]);
     int issued = pre;
     bool ok = true;
     for (int kb = pre; kb < nk && ok; ++kb) {
@@ -244,8 +249,9 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
       }
       uint8_t* sa = smem + (size_t)s * stage_bytes;
       mbar_expect_tx(&full_bar[s], (uint32_t)stage_bytes);
-      tma_load_2d(sa, &map_w, kb * kBK, m0, &full_bar[s]);
-      tma_load_2d(sa + kABytes, &map_h, kb * kBK, 0, &full_bar[s]);
+      const int x = ((kb + rot) % nk) * kBK;
+      tma_load_2d(sa, &map_w, x, m0, &full_bar[s]);
+      tma_load_2d(sa + kABytes, &map_h, x, 0, &full_bar[s]);
       issued = kb + 1;
     }
     if (!ok) atomicExch(&s_err, 1);

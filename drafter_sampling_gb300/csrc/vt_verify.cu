@@ -393,29 +393,43 @@ __global__ void __launch_bounds__(kNT, 8) verify_finish_kernel(VArgs a) {
     __threadfence();
   }
 
-  // 4. last tile of sequence b to finish: choose the tile, then the token
+  // 4. last tile of sequence b to finish: choose the tile, then the token.
+  // Thread t sums the consecutive tiles [t * per, (t + 1) * per) in order;
+  // one block scan of those sums gives every running sum the choice needs.
   int glast = -1;
   for (int k = tid; k < a.C2; k += kNT) {
     sm.zbuf[k] = __ldcg(a.zpart + (int64_t)b * a.C2 + k);
     glast = max(glast, __ldcg(a.lpart + (int64_t)b * a.C2 + k));
   }
-  glast = block_max_int<kNT>(glast, sm.ired);
-  if (tid == 0) {
-    float total = 0.f;
-    for (int k = 0; k < a.C2; ++k) total += sm.zbuf[k];
-    const float target = a.u_res[(int64_t)b * R + n] * total;
-    float pre = 0.f;
-    int cstar = -1;
-    if (total > 0.f) {
-      for (int k = 0; k < a.C2; ++k) {
-        if (pre + sm.zbuf[k] > target) { cstar = k; break; }
+  const float ures = a.u_res[(int64_t)b * R + n];
+  glast = block_max_int<kNT>(glast, sm.ired);  // also publishes zbuf
+  {
+    const int per = (a.C2 + kNT - 1) / kNT;
+    const int k0 = tid * per, k1 = min(a.C2, k0 + per);
+    float mine = 0.f;
+    for (int k = k0; k < k1; ++k) mine += sm.zbuf[k];
+    float excl, total;
+    const float incl = block_scan_incl<kNT>(mine, sm.sred, excl, total);
+    const float target = ures * total;
+    const int first = block_min_int<kNT>((total > 0.f && incl > target) ? tid : kNT, sm.ired);
+    if (tid == 0) {
+      sm.cstar = (total > 0.f) ? -1 : -2;  // -1: rounding put u * Z past every sum
+      sm.target = 0.f;
+    }
+    __syncthreads();
+    if (tid == first) {
+      float pre = excl;
+      for (int k = k0; k < k1; ++k) {
+        if (pre + sm.zbuf[k] > target) {
+          sm.cstar = k;
+          sm.target = target - pre;
+          break;
+        }
         pre += sm.zbuf[k];
       }
     }
-    sm.cstar = (total > 0.f) ? cstar : -2;
-    sm.target = target - pre;
+    __syncthreads();
   }
-  __syncthreads();
   int token = glast;
   int extra = 0;
   if (sm.cstar >= 0) {
@@ -437,7 +451,7 @@ __global__ void __launch_bounds__(kNT, 8) verify_finish_kernel(VArgs a) {
       total += tot;
     }
     __syncthreads();
-    const float target = a.u_res[(int64_t)b * R + n] * total;
+    const float target = ures * total;
     float pre = 0.f;
     int cstar = a.C2 - 1;
     for (int k = 0; k < a.C2; ++k) {
