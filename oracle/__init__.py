@@ -45,9 +45,19 @@ pages or the mathematics fix (none is "parity unpinned"):
 * draft_step             two-token softmax and sampling edges; equality with
                          the masked full-vocabulary head; chi-square of draws
                          (tests/test_oracle_vocabtrim.py)
+* argmax_lowest          hand-worked ties; numpy argmax on distinct values
+* draft_step_greedy      exact rational dot products; the sampling draft at a
+                         vanishing temperature
+* verify_greedy          lossless: chained greedy speculative decoding emits
+                         exactly the target's own greedy stream on the toy
+                         tables; equals the stochastic verify at a vanishing
+                         temperature for any uniforms; hand-worked blocks
+                         (tests/test_oracle_greedy.py)
 """
 from .sampling import inverse_cdf, InverseCdfResult  # noqa: F401
 from .vocabtrim import (token_histogram, top_k, trim_head, bf16_to_f64,  # noqa: F401
                         draft_logits, draft_step, BadInput)
 from .speculative import (softmax, acceptance_probability, residual_weights,  # noqa: F401
                           verify, VerifyResult)
+from .greedy import (argmax_lowest, top2_gap, draft_step_greedy, verify_greedy,  # noqa: F401
+                     GreedyResult)
