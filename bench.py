@@ -498,6 +498,7 @@ def main():
         "gpu_launches": sum(KERNELS_PER_CALL[r] * CALLS_PER_STEP[r] for r in ROWS) * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "dev_status": status,
+        "next_rows": {"greedy_block": run_greedy_block(torch, vt, step)},
     }
 
     if not args.no_e2e:
@@ -513,6 +514,45 @@ def main():
     if rank == 0:
         print(json.dumps(line))
     return 0
+
+
+def run_greedy_block(torch, vt, step, nblocks: int = 100):
+    """Greedy (temperature 0) block on the step's tensors: six greedy draft
+    steps (argmax through the trimmed head, one-hot q) and greedy
+    verification (argmax of every target row).  Timed back to back with one
+    event pair around all blocks; the drafts reuse the calibrated W_trim."""
+    s = step.vsets[0]
+
+    def block():
+        for j in range(GAMMA):
+            vt.vt_draft_step(step.hidden[j], step.W_trim, step.trim_ids, None, 0.0,
+                             q=step.q[:, j, :], tokens=step.tokens[:, j],
+                             dev_status=step.status[2:3], workspace=step.ws_draft)
+        vt.vt_verify(s["logits"], None, None, step.tokens, None, None, 0.0,
+                     out_tokens=step.out_tokens, out_num_accepted=step.out_n,
+                     out_accept_prob=step.out_acc, dev_status=step.status[3:4],
+                     workspace=step.ws_ver)
+
+    for _ in range(3):
+        block()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(nblocks):
+        block()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / nblocks
+    alg = algorithmic_bytes()
+    # greedy verify reads the logits once (no q, no residual row)
+    bytes_block = GAMMA * alg["draft"] + B * (GAMMA + 1) * V * 4
+    status = [int(x) for x in step.status[2:4].cpu().tolist()]
+    return {"value": B * GAMMA / (us * 1e-6), "unit": UNIT, "us_per_block": us,
+            "algorithmic_bytes_per_block": bytes_block,
+            "achieved_gbs": bytes_block / (us * 1e-6) / 1e9,
+            "mean_accepted": float(step.out_n.float().mean().item()), "dev_status": status,
+            "note": "temperature 0: greedy drafting and verification, calibrate/trim excluded"}
 
 
 def run_e2e(torch, step, host, stream, args, dist, dev, world):

@@ -169,13 +169,16 @@ def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, 
 
     ``q`` may be a strided view such as q_all[:, pos, :] of a contiguous
     [B, gamma, K] tensor (unit inner stride), and ``tokens`` a strided view
-    such as tok_all[:, pos] of a [B, gamma] tensor.
+    such as tok_all[:, pos] of a [B, gamma] tensor.  temperature == 0 drafts
+    greedily (q one-hot); ``uniforms`` may then be None.
     """
     torch = _torch()
+    greedy = float(temperature) == 0.0
     _dev(hidden, "hidden", _bf16_dtypes(), 2)
     _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
     _dev(trim_ids, "trim_ids", (torch.int32,), 1)
-    _dev(uniforms, "uniforms", (torch.float32,), 1)
+    if uniforms is not None or not greedy:
+        _dev(uniforms, "uniforms", (torch.float32,), 1)
     B, H = hidden.shape
     K = W_trim.shape[0]
     dev = hidden.device
@@ -189,13 +192,14 @@ def vt_draft_step(hidden, W_trim, trim_ids, uniforms, temperature: float = 1.0, 
         raise ValueError("tokens must be an int32 vector of B entries (any stride)")
     if dev_status is None:
         dev_status = torch.empty(1, dtype=torch.int32, device=dev)
-    if uniforms.numel() != B or trim_ids.numel() != K:
+    if (uniforms is not None and uniforms.numel() != B) or trim_ids.numel() != K:
         raise ValueError("uniforms must have B and trim_ids K elements")
     L = lib()
     if workspace is None:
         workspace = _ws(L.vt_draft_workspace_bytes(B, H, K), dev)
     st = L.vt_draft_step(hidden.data_ptr(), B, H, W_trim.data_ptr(), trim_ids.data_ptr(), K,
-                         uniforms.data_ptr(), float(temperature), q.data_ptr(), q.stride(0),
+                         uniforms.data_ptr() if uniforms is not None else None,
+                         float(temperature), q.data_ptr(), q.stride(0),
                          tokens.data_ptr(), tokens.stride(0), dev_status.data_ptr(),
                          workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _lib.check("vt_draft_step", st)
@@ -209,6 +213,8 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
     """Modified rejection sampling over a batch of drafted blocks.
 
     target_logits [B, gamma+1, V] float32 or bf16; q [B, gamma, K] float32.
+    temperature == 0 verifies greedily (a drafted token is kept iff it is the
+    target's highest logit); q, inv_map and the uniforms may then be None.
     Returns (out_tokens [B, gamma+1], out_num_accepted [B], out_accept_prob
     [B, gamma] or None, dev_status [1]).
     """
@@ -219,21 +225,27 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
         dt = VT_BF16
     else:
         raise TypeError("target_logits must be float32 or bf16")
+    greedy = float(temperature) == 0.0
     _dev(target_logits, "target_logits", (target_logits.dtype,), 3)
-    _dev(q, "q", (torch.float32,), 3)
-    _dev(inv_map, "inv_map", (torch.int32,), 1)
     _dev(draft_tokens, "draft_tokens", (torch.int32,), 2)
-    _dev(u_accept, "u_accept", (torch.float32,), 2)
-    _dev(u_resample, "u_resample", (torch.float32,), 2)
     B, R, V = target_logits.shape
     gamma = R - 1
-    K = q.shape[2]
-    if tuple(q.shape[:2]) != (B, gamma) or tuple(draft_tokens.shape) != (B, gamma):
-        raise ValueError("q / draft_tokens shapes do not match target_logits")
-    if tuple(u_accept.shape) != (B, gamma) or tuple(u_resample.shape) != (B, R):
-        raise ValueError("uniform shapes do not match")
-    if inv_map.numel() != V:
-        raise ValueError("inv_map must have V entries")
+    if tuple(draft_tokens.shape) != (B, gamma):
+        raise ValueError("draft_tokens shape does not match target_logits")
+    given = [x is not None for x in (q, inv_map, u_accept, u_resample)]
+    if not greedy or any(given):
+        _dev(q, "q", (torch.float32,), 3)
+        _dev(inv_map, "inv_map", (torch.int32,), 1)
+        _dev(u_accept, "u_accept", (torch.float32,), 2)
+        _dev(u_resample, "u_resample", (torch.float32,), 2)
+        if tuple(q.shape[:2]) != (B, gamma):
+            raise ValueError("q shape does not match target_logits")
+        if tuple(u_accept.shape) != (B, gamma) or tuple(u_resample.shape) != (B, R):
+            raise ValueError("uniform shapes do not match")
+        if inv_map.numel() != V:
+            raise ValueError("inv_map must have V entries")
+    K = q.shape[2] if q is not None else 1
+    ptr = lambda x: x.data_ptr() if x is not None else None
     dev = target_logits.device
     if out_tokens is None:
         out_tokens = torch.empty((B, R), dtype=torch.int32, device=dev)
@@ -246,8 +258,8 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
     L = lib()
     if workspace is None:
         workspace = _ws(L.vt_verify_workspace_bytes(B, gamma, V, K), dev)
-    st = L.vt_verify(target_logits.data_ptr(), dt, B, gamma, V, q.data_ptr(), inv_map.data_ptr(),
-                     K, draft_tokens.data_ptr(), u_accept.data_ptr(), u_resample.data_ptr(),
+    st = L.vt_verify(target_logits.data_ptr(), dt, B, gamma, V, ptr(q), ptr(inv_map),
+                     K, draft_tokens.data_ptr(), ptr(u_accept), ptr(u_resample),
                      float(temperature), out_tokens.data_ptr(), out_num_accepted.data_ptr(),
                      out_accept_prob.data_ptr() if out_accept_prob is not None else None,
                      dev_status.data_ptr(), workspace.data_ptr(), workspace.numel(),

@@ -59,7 +59,7 @@ draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
                   const uint16_t* __restrict__ W, int K, float out_scale,
                   float* __restrict__ out, int64_t ldo, float2* __restrict__ part,
                   int* __restrict__ zero_ints, int nzero, int* __restrict__ status_to_zero,
-                  int vec_ok) {
+                  int vec_ok, int greedy) {
   extern __shared__ __align__(16) uint16_t sh_h[];  // [BT][H]
   __shared__ MS sred[kGemvNT / 32][BT];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -95,7 +95,10 @@ draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
 
     float m[BT], s[BT];
 #pragma unroll
-    for (int b = 0; b < BT; ++b) { m[b] = kNegBig; s[b] = 0.f; }
+    for (int b = 0; b < BT; ++b) {
+      m[b] = greedy ? -INFINITY : kNegBig;
+      s[b] = greedy ? __int_as_float(0x7fffffff) : 0.f;
+    }
 
     const int groups = (K + kRowsPerWarp - 1) / kRowsPerWarp;
     // one group of 8 consecutive rows per warp: CTA g covers rows [64g, 64g+64)
@@ -174,11 +177,20 @@ draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
           if (b < bt) {
             const float z = acc[b] * out_scale;
             out[(int64_t)(b0 + b) * ldo + row] = z;
-            if (z > m[b]) {
-              s[b] *= exp2_approx(m[b] - z);
-              m[b] = z;
+            if (greedy) {
+              // m = max z, s = its lowest row (rows rise along this loop)
+              const float v = isfinite(z) ? z : __int_as_float(0x7fc00000);
+              if (umma::argmax_better(m[b], __float_as_int(s[b]), v, row)) {
+                m[b] = v;
+                s[b] = __int_as_float(row);
+              }
+            } else {
+              if (z > m[b]) {
+                s[b] *= exp2_approx(m[b] - z);
+                m[b] = z;
+              }
+              s[b] += exp2_approx(z - m[b]);
             }
-            s[b] += exp2_approx(z - m[b]);
           }
         }
       }
@@ -186,14 +198,29 @@ draft_gemv_kernel(const uint16_t* __restrict__ hidden, int B, int H,
     if (part != nullptr) {
 #pragma unroll
       for (int b = 0; b < BT; ++b) {
-        MS v = warp_ms_reduce(MS{m[b], s[b]});
-        if (lane == 0) sred[warp][b] = v;
+        if (greedy) {
+          float v = m[b];
+          int i = __float_as_int(s[b]);
+          umma::warp_argmax(v, i);
+          if (lane == 0) sred[warp][b] = MS{v, __int_as_float(i)};
+        } else {
+          MS v = warp_ms_reduce(MS{m[b], s[b]});
+          if (lane == 0) sred[warp][b] = v;
+        }
       }
       __syncthreads();
       if (tid < bt) {
         MS r = sred[0][tid];
 #pragma unroll
-        for (int w = 1; w < kGemvNT / 32; ++w) r = ms_combine(r, sred[w][tid]);
+        for (int w = 1; w < kGemvNT / 32; ++w) {
+          if (greedy) {
+            if (umma::argmax_better(r.m, __float_as_int(r.s), sred[w][tid].m,
+                                    __float_as_int(sred[w][tid].s)))
+              r = sred[w][tid];
+          } else {
+            r = ms_combine(r, sred[w][tid]);
+          }
+        }
         part[(int64_t)blockIdx.x * B + b0 + tid] = make_float2(r.m, r.s);
       }
     }
@@ -374,6 +401,72 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
 }
 
+struct GreedyFinArgs {
+  float* q;            // in: raw logits z; out: one-hot at the greedy index
+  int64_t ldq;
+  int B, K;
+  const float2* part;  // [G][B] (max z, its lowest row) of consecutive row tiles
+  int G;
+  const int* trim_ids;
+  int* tokens;
+  int64_t ldt;
+  int* dev_status;
+  int vec_ok;
+};
+
+// Greedy drafting (temperature 0): j* = the largest z of row b, ties to the
+// lower trimmed index, from the projection's per-tile (max, row) partials;
+// q[b, :] = one-hot at j*; token = trim_ids[j*].  Grid (B, chunks of 1024
+// ids): every CTA merges the partials itself and writes its chunk of q.
+__global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFinArgs a) {
+  __shared__ float sv[kFinNT / 32];
+  __shared__ int si[kFinNT / 32];
+  const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  griddep_launch_dependents();  // the next kernel waits for this grid before reading
+  griddep_wait();               // the projection has completed
+  float v = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int t = tid; t < a.G; t += kFinNT) {
+    const float2 p = a.part[(int64_t)t * a.B + b];
+    const int pi = __float_as_int(p.y);
+    if (umma::argmax_better(v, idx, p.x, pi)) {
+      v = p.x;
+      idx = pi;
+    }
+  }
+  umma::warp_argmax(v, idx);
+  if (lane == 0) {
+    sv[warp] = v;
+    si[warp] = idx;
+  }
+  __syncthreads();
+  v = sv[0];
+  idx = si[0];
+  for (int w = 1; w < kFinNT / 32; ++w)
+    if (umma::argmax_better(v, idx, sv[w], si[w])) {
+      v = sv[w];
+      idx = si[w];
+    }
+  const bool ok = (v == v) && idx >= 0 && idx < a.K;  // NaN: a non-finite z was seen
+  float* qrow = a.q + (int64_t)b * a.ldq;
+  const int64_t j = (int64_t)c * kFinChunk + 4 * (int64_t)tid;
+  float o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] = (ok && j + e == idx) ? 1.f : 0.f;
+  if (a.vec_ok && j + 3 < a.K) {
+    *reinterpret_cast<float4*>(qrow + j) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e < a.K) qrow[j + e] = o[e];
+  }
+  if (c == 0 && tid == 0) {
+    a.tokens[(int64_t)b * a.ldt] = ok ? a.trim_ids[idx] : -1;
+    if (!ok) atomicOr(a.dev_status, VT_DEV_NONFINITE);
+  }
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -426,7 +519,7 @@ template <int BT>
 cudaError_t launch_gemv_bt(int grid, cudaStream_t s, const uint16_t* hidden, int B, int H,
                            const uint16_t* W, int K, float out_scale, float* out, int64_t ldo,
                            float2* part, int* zero_ints, int nzero, int* status_to_zero,
-                           int vec_ok) {
+                           int vec_ok, int greedy) {
   const size_t smem = (size_t)BT * H * sizeof(uint16_t);
   auto kern = draft_gemv_kernel<BT, 4>;
   if (smem > 48 * 1024) {
@@ -434,13 +527,13 @@ cudaError_t launch_gemv_bt(int grid, cudaStream_t s, const uint16_t* hidden, int
     if (e != cudaSuccess) return e;
   }
   kern<<<grid, kGemvNT, smem, s>>>(hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
-                                   status_to_zero, vec_ok);
+                                   status_to_zero, vec_ok, greedy);
   return cudaGetLastError();
 }
 
 int launch_gemv(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints,
-                int nzero, int* status_to_zero, int* grid_out) {
+                int nzero, int* status_to_zero, int greedy, int* grid_out) {
   const int vec_ok = (H % 8 == 0) && ((reinterpret_cast<uintptr_t>(hidden) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
   int bt = gemv_bt(B);
@@ -453,11 +546,11 @@ int launch_gemv(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   *grid_out = grid;
   cudaError_t e;
   switch (bt) {
-    case 16: e = launch_gemv_bt<16>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
-    case 8: e = launch_gemv_bt<8>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
-    case 4: e = launch_gemv_bt<4>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
-    case 2: e = launch_gemv_bt<2>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
-    default: e = launch_gemv_bt<1>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok); break;
+    case 16: e = launch_gemv_bt<16>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok, greedy); break;
+    case 8: e = launch_gemv_bt<8>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok, greedy); break;
+    case 4: e = launch_gemv_bt<4>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok, greedy); break;
+    case 2: e = launch_gemv_bt<2>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok, greedy); break;
+    default: e = launch_gemv_bt<1>(grid, s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status_to_zero, vec_ok, greedy); break;
   }
   return e == cudaSuccess ? VT_OK : VT_ERR_CUDA;
 }
@@ -525,7 +618,7 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
 // z = out_scale * hidden @ W^T on the tensor cores; part[tile][b] partials
 int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
-                int* status, int status_reset, int* groups_out) {
+                int* status, int status_reset, int greedy, int* groups_out) {
   const int BN = (B <= 16) ? 16 : (B <= 32) ? 32 : (B <= 64) ? 64 : (B <= 128) ? 128 : 256;
   CUtensorMap mw, mh;
   if (!make_bf16_map(&mw, W, (uint64_t)K, (uint64_t)H, umma::kBM)) return VT_ERR_CUDA;
@@ -543,6 +636,7 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   a.status = status;
   a.status_reset = status_reset;
   a.stages = 2;
+  a.greedy = greedy;
   const int tiles = (K + umma::kBM - 1) / umma::kBM;
   *groups_out = tiles;
   switch (BN) {
@@ -557,22 +651,23 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
 // the projection through whichever engine the shapes allow
 int launch_head(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
-                int* status, int status_reset, int* groups_out, int* tile_rows_out) {
+                int* status, int status_reset, int greedy, int* groups_out, int* tile_rows_out) {
   if (umma_supported(hidden, B, H, W)) {
     *tile_rows_out = umma::kBM;
     return launch_umma(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status,
-                       status_reset, groups_out);
+                       status_reset, greedy, groups_out);
   }
   *tile_rows_out = kGemvRowTile;
   return launch_gemv(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
-                     status_reset ? status : nullptr, groups_out);
+                     status_reset ? status : nullptr, greedy, groups_out);
 }
 
+// T > 0, or T == 0 where greedy drafting is allowed
 int check_draft_args(const uint16_t* hidden, int B, int H, const uint16_t* W_trim, int K,
-                     float T) {
+                     float T, bool allow_greedy) {
   if (!hidden || !W_trim) return VT_ERR_INVALID_ARG;
   if (B < 1 || B > 4096 || H < 1 || H > 65536 || K < 1) return VT_ERR_INVALID_ARG;
-  if (!(T > 0.f) || !std::isfinite(T)) return VT_ERR_INVALID_ARG;
+  if (!std::isfinite(T) || T < 0.f || (T == 0.f && !allow_greedy)) return VT_ERR_INVALID_ARG;
   return VT_OK;
 }
 
@@ -590,7 +685,7 @@ extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
                                float* logits, int64_t ld_logits, void* workspace,
                                size_t workspace_bytes, void* stream) {
   using namespace vt;
-  int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
+  int st = check_draft_args(hidden, B, H, W_trim, K, temperature, false);
   if (st != VT_OK) return st;
   if (!logits || ld_logits < K) return VT_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
@@ -598,7 +693,7 @@ extern "C" int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   int groups = 0, tile_rows = 0;
   return launch_head(static_cast<cudaStream_t>(stream), hidden, B, H, W_trim, K,
-                     1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, ws.status_sink, 1,
+                     1.0f / temperature, logits, ld_logits, nullptr, nullptr, 0, ws.status_sink, 1, 0,
                      &groups, &tile_rows);
 }
 
@@ -608,9 +703,11 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                              int32_t* tokens, int64_t ld_tokens, int32_t* dev_status,
                              void* workspace, size_t workspace_bytes, void* stream) {
   using namespace vt;
-  int st = check_draft_args(hidden, B, H, W_trim, K, temperature);
+  int st = check_draft_args(hidden, B, H, W_trim, K, temperature, true);
   if (st != VT_OK) return st;
-  if (!trim_ids || !uniforms || !q || ldq < K || !tokens || ld_tokens < 1 || !dev_status)
+  const bool greedy = temperature == 0.f;
+  if (!trim_ids || (!uniforms && !greedy) || !q || ldq < K || !tokens || ld_tokens < 1 ||
+      !dev_status)
     return VT_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   DraftWs ws = carve_draft(workspace, B, K);
@@ -620,9 +717,34 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   // the projection zeroes the status word (its first CTA runs before the
   // finalize grid starts: same stream)
   int grid = 0, tile_rows = 0;
-  st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, q, ldq, ws.part, nullptr, 0,
-                   dev_status, 1, &grid, &tile_rows);
+  st = launch_head(s, hidden, B, H, W_trim, K, greedy ? 1.0f : VT_LOG2E / temperature, q, ldq,
+                   ws.part, nullptr, 0, dev_status, 1, greedy ? 1 : 0, &grid, &tile_rows);
   if (st != VT_OK) return st;
+  if (greedy) {
+    GreedyFinArgs ga;
+    ga.q = q;
+    ga.ldq = ldq;
+    ga.B = B;
+    ga.K = K;
+    ga.part = ws.part;
+    ga.G = grid;
+    ga.trim_ids = trim_ids;
+    ga.tokens = tokens;
+    ga.ldt = ld_tokens;
+    ga.dev_status = dev_status;
+    ga.vec_ok = ((reinterpret_cast<uintptr_t>(q) & 15) == 0) && (ldq % 4 == 0);
+    cudaLaunchConfig_t gcfg = {};
+    gcfg.gridDim = dim3((unsigned)B, (unsigned)((K + kFinChunk - 1) / kFinChunk));
+    gcfg.blockDim = dim3(kFinNT);
+    gcfg.stream = s;
+    cudaLaunchAttribute gattr[1];
+    gattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    gattr[0].val.programmaticStreamSerializationAllowed = 1;
+    gcfg.attrs = gattr;
+    gcfg.numAttrs = 1;
+    VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&gcfg, draft_greedy_finalize_kernel, ga));
+    return VT_OK;
+  }
 
   FinArgs fa;
   fa.q = q;

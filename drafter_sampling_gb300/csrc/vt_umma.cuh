@@ -10,7 +10,8 @@
 // tensor memory, fp32), one thread issues the TMA loads, and all four warps
 // read the accumulator back (tcgen05.ld, one TMEM lane quarter per warp) to
 // scale and store z and fold each tile's rows into per-batch-row online-
-// softmax partials (max, sum 2^(z - max)).
+// softmax partials (max, sum 2^(z - max)), or, for greedy drafting, into
+// (max z, the lowest row holding it).
 //
 // The first ring stages of W_trim are requested before the kernel waits on
 // the previous kernel in the stream (programmatic dependent launch); the
@@ -172,7 +173,27 @@ struct HeadArgs {
   int* status;       // zeroed by CTA 0 when status_reset, VT_DEV_TIMEOUT on expiry
   int status_reset;
   int stages;
+  int greedy;        // part holds (max z, its lowest row) instead of (max, sum 2^(z-max))
 };
+
+// (value, index) pairs of an argmax, ties to the lower index; a NaN value
+// (non-finite input seen) wins every comparison so it reaches the result
+__device__ __forceinline__ bool argmax_better(float v, int i, float w, int k) {
+  if (v != v) return false;
+  if (w != w) return true;
+  return w > v || (w == v && k < i);
+}
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    const int k = __shfl_xor_sync(0xffffffffu, i, o);
+    if (argmax_better(v, i, w, k)) {
+      v = w;
+      i = k;
+    }
+  }
+}
 
 // one CTA per 128-row tile of W_trim; BN = padded batch (16..256, step 16)
 template <int BN>
@@ -305,7 +326,12 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int b = c0 + e;
         const float z = v[e] * a.out_scale;
         if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
-        if (a.part != nullptr) {
+        if (a.part != nullptr && a.greedy) {
+          float v = (j < a.K) ? (isfinite(z) ? z : __int_as_float(0x7fc00000)) : -INFINITY;
+          int idx = (j < a.K) ? j : 0x7fffffff;
+          warp_argmax(v, idx);
+          if (lane == 0) red[warp][b] = MS{v, __int_as_float(idx)};
+        } else if (a.part != nullptr) {
           MS m = (j < a.K) ? MS{z, 1.f} : MS{kNegBig, 0.f};
           m = warp_ms_reduce(m);
           if (lane == 0) red[warp][b] = m;
@@ -320,10 +346,24 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   if (a.part != nullptr && acc_ok) {
     for (int b = tid; b < a.B && b < BN; b += kThreads) {
       MS r = red[0][b];
-      r = ms_combine(r, red[1][b]);
-      r = ms_combine(r, red[2][b]);
-      r = ms_combine(r, red[3][b]);
-      a.part[(int64_t)tile * a.B + b] = make_float2(r.m, r.s);
+      if (a.greedy) {
+        float v = r.m;
+        int idx = __float_as_int(r.s);
+        for (int w = 1; w < 4; ++w) {
+          const float wv = red[w][b].m;
+          const int wi = __float_as_int(red[w][b].s);
+          if (argmax_better(v, idx, wv, wi)) {
+            v = wv;
+            idx = wi;
+          }
+        }
+        a.part[(int64_t)tile * a.B + b] = make_float2(v, __int_as_float(idx));
+      } else {
+        r = ms_combine(r, red[1][b]);
+        r = ms_combine(r, red[2][b]);
+        r = ms_combine(r, red[3][b]);
+        a.part[(int64_t)tile * a.B + b] = make_float2(r.m, r.s);
+      }
     }
   }
   if (tid == 0 && s_err) atomicOr(a.status, VT_DEV_TIMEOUT);

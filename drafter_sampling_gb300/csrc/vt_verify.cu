@@ -522,6 +522,167 @@ int launch_verify(const VArgs& a, cudaStream_t s) {
   return VT_OK;
 }
 
+// ------------------------------------------------- greedy (temperature 0)
+// VocabTrim's greedy setting (section 4, Algorithm 2): position i keeps the
+// drafted x_i iff it is the largest logit of row i (ties to the lower id);
+// the first mismatch is replaced by that row's choice, and a fully accepted
+// block appends the choice at position gamma.  The logits are compared as
+// given (fp32, or bf16 widened exactly), so the choices are exact.
+
+// (value, index) argmax, ties to the lower index; NaN (a non-finite logit)
+// wins every comparison so it reaches the result
+__device__ __forceinline__ bool gbetter(float v, int i, float w, int k) {
+  if (v != v) return false;
+  if (w != w) return true;
+  return w > v || (w == v && k < i);
+}
+
+__device__ __forceinline__ void warp_gmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    const int k = __shfl_xor_sync(0xffffffffu, i, o);
+    if (gbetter(v, i, w, k)) {
+      v = w;
+      i = k;
+    }
+  }
+}
+
+// grid (rows, C1 chunks): per chunk the largest logit and its lowest id
+template <typename T>
+__global__ void __launch_bounds__(kNT) verify_greedy_stats_kernel(VArgs a) {
+  __shared__ float sv[kNT / 32];
+  __shared__ int si[kNT / 32];
+  constexpr int VEC = Elem<T>::kVec;
+  constexpr int U = kStatsBytes / 16 / kNT;
+  griddep_wait();
+  const int64_t row = blockIdx.x;
+  const int c = blockIdx.y;
+  if (row == 0 && c == 0 && threadIdx.x == 0) *a.dev_status = 0;
+  const T* rp = static_cast<const T*>(a.logits) + row * a.V;
+  const int64_t j0 = (int64_t)c * a.len1;
+  const int64_t j1 = min(a.V, j0 + a.len1);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  // this thread's ids rise along both loops, so a tie keeps the lower id
+  auto take = [&](float x, int64_t j) {
+    const float v = isfinite(x) ? x : __int_as_float(0x7fc00000);
+    if (gbetter(bv, bi, v, (int)j)) {
+      bv = v;
+      bi = (int)j;
+    }
+  };
+  int64_t jt = j0;
+  if (a.vec_ok) {
+    const int64_t nv = (j1 - j0) / VEC;
+    const uint4* vp = reinterpret_cast<const uint4*>(rp + j0);
+    for (int64_t v = threadIdx.x; v < nv; v += (int64_t)kNT * U) {
+      uint4 raw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t vi = v + (int64_t)u * kNT;
+        if (vi < nv) raw[u] = __ldg(vp + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t vi = v + (int64_t)u * kNT;
+        if (vi < nv) {
+          float x[VEC];
+          Elem<T>::unpack16(raw[u], x);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) take(x[e], j0 + vi * VEC + e);
+        }
+      }
+    }
+    jt = j0 + nv * VEC;
+  }
+  for (int64_t j = jt + threadIdx.x; j < j1; j += kNT) take(Elem<T>::load(rp + j), j);
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_gmax(bv, bi);
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kNT / 32; ++w)
+      if (gbetter(bv, bi, sv[w], si[w])) {
+        bv = sv[w];
+        bi = si[w];
+      }
+    a.part[row * a.C1 + c] = make_float2(bv, __int_as_float(bi));
+  }
+}
+
+// grid (B): merge the chunk partials of the gamma+1 rows, walk, write
+__global__ void __launch_bounds__(kNT) verify_greedy_finish_kernel(VArgs a) {
+  __shared__ int choice[kMaxGamma + 1];
+  __shared__ unsigned fail[2];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.R;
+  griddep_wait();  // the stats kernel has completed
+  for (int i = warp; i < R; i += kNT / 32) {
+    float v = -INFINITY;
+    int idx = 0x7fffffff;
+    const float2* pp = a.part + ((int64_t)b * R + i) * a.C1;
+    for (int k = lane; k < a.C1; k += 32) {
+      const float2 t = pp[k];
+      if (gbetter(v, idx, t.x, __float_as_int(t.y))) {
+        v = t.x;
+        idx = __float_as_int(t.y);
+      }
+    }
+    warp_gmax(v, idx);
+    if (lane == 0) choice[i] = (v == v && idx >= 0 && (int64_t)idx < a.V) ? idx : -1;
+  }
+  __syncthreads();
+  bool bad = false;
+  if (tid < 64) {
+    bool f = false;
+    if (tid < a.gamma) {
+      const int x = a.draft[(int64_t)b * a.gamma + tid];
+      bad = !(x >= 0 && (int64_t)x < a.V);
+      f = bad || x != choice[tid];
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) fail[warp] = bal;
+  }
+  __syncthreads();
+  const uint64_t mask = (uint64_t)fail[0] | ((uint64_t)fail[1] << 32);
+  const int n = mask ? (__ffsll((long long)mask) - 1) : a.gamma;
+  int flags = 0;
+  for (int i = 0; i < R; ++i)
+    if (choice[i] < 0) flags |= VT_DEV_NONFINITE;
+  // a drafted token outside [0, V) stops the walk at its position
+  if (__syncthreads_or(tid == n && tid < a.gamma && bad)) flags |= VT_DEV_BAD_DRAFT;
+  if (a.out_accept_prob != nullptr && tid < a.gamma)
+    a.out_accept_prob[(int64_t)b * a.gamma + tid] =
+        (flags == 0 && tid <= n) ? (tid < n ? 1.f : 0.f) : __int_as_float(0x7fc00000);
+  for (int i = tid; i < R; i += kNT) {
+    int v = -1;
+    if (flags == 0) {
+      if (i < n) v = a.draft[(int64_t)b * a.gamma + i];
+      else if (i == n) v = choice[n];
+    }
+    a.out_tokens[(int64_t)b * R + i] = v;
+  }
+  if (tid == 0) {
+    a.out_n[b] = flags ? 0 : n;
+    if (flags) atomicOr(a.dev_status, flags);
+  }
+}
+
+template <typename T>
+int launch_verify_greedy(const VArgs& a, cudaStream_t s) {
+  VT_RETURN_IF_CUDA(launch_pdl(verify_greedy_stats_kernel<T>,
+                               dim3((unsigned)((int64_t)a.B * a.R), (unsigned)a.C1), s, a));
+  VT_RETURN_IF_CUDA(launch_pdl(verify_greedy_finish_kernel, dim3((unsigned)a.B), s, a));
+  return VT_OK;
+}
+
+
 }  // namespace
 }  // namespace vt
 
@@ -538,14 +699,16 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
                          int32_t* out_num_accepted, float* out_accept_prob, int32_t* dev_status,
                          void* workspace, size_t workspace_bytes, void* stream) {
   using namespace vt;
-  if (!target_logits || !q || !inv_map || !draft_tokens || !u_accept || !u_resample ||
-      !out_tokens || !out_num_accepted || !dev_status)
+  // temperature 0: greedy verification (q, inv_map and the uniforms are not read)
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !dev_status)
     return VT_ERR_INVALID_ARG;
+  if (!greedy && (!q || !inv_map || !u_accept || !u_resample)) return VT_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || gamma < 1 || gamma > kMaxGamma || V < 1 || K < 1 || K > V ||
       V > (1 << 22))
     return VT_ERR_INVALID_ARG;
   if (logits_dtype != VT_F32 && logits_dtype != VT_BF16) return VT_ERR_INVALID_ARG;
-  if (!(temperature > 0.f) || !std::isfinite(temperature)) return VT_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return VT_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   const VerifyLayout L = verify_layout(B, gamma, V);
   if (workspace_bytes < L.bytes) return VT_ERR_WORKSPACE;
@@ -565,7 +728,7 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
   a.draft = draft_tokens;
   a.u_acc = u_accept;
   a.u_res = u_resample;
-  a.scale = VT_LOG2E / temperature;
+  a.scale = greedy ? 1.f : VT_LOG2E / temperature;
   // stats chunks of 32 KB (at most kMaxChunks1 per row), aligned to the
   // 16-byte vector width
   int64_t len1 = std::max<int64_t>(kStatsBytes / (int64_t)esize,
@@ -588,6 +751,10 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
   a.out_accept_prob = out_accept_prob;
   a.dev_status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (greedy) {
+    if (logits_dtype == VT_F32) return launch_verify_greedy<float>(a, s);
+    return launch_verify_greedy<uint16_t>(a, s);
+  }
   if (logits_dtype == VT_F32) return launch_verify<float>(a, s);
   return launch_verify<uint16_t>(a, s);
 }
@@ -641,9 +808,11 @@ extern "C" int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype
   if (B < 1 || gamma < 1 || gamma > kMaxGamma) return VT_ERR_INVALID_ARG;
   const size_t need = vt_verify_workspace_bytes(B, gamma, V, K);
   if (need > VT_VERIFY_NOALLOC_SCRATCH_BYTES) return VT_ERR_SCRATCH_LIMIT;
-  if (!target_logits || !q || !inv_map || !draft_tokens || !u_accept || !u_resample ||
-      !out_tokens || !out_num_accepted || !dev_status)
+  // temperature 0: greedy verification (q, inv_map and the uniforms are not read)
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !dev_status)
     return VT_ERR_INVALID_ARG;
+  if (!greedy && (!q || !inv_map || !u_accept || !u_resample)) return VT_ERR_INVALID_ARG;
   void* scratch = nullptr;
   const int st = noalloc_scratch_address(&scratch);
   if (st != VT_OK) return st;

@@ -158,6 +158,11 @@ int vt_draft_logits(const uint16_t* hidden, int32_t B, int32_t H,
  *                            (pass ld_tokens = gamma and tokens + pos to fill
  *                            column `pos` of a [B, gamma] tensor; ld_tokens >= 1)
  *  dev_status int32 [1]      out: VT_DEV_NONFINITE
+ * T == 0 drafts greedily ([VT] section 4 decodes greedily; Algorithm 2):
+ * j* = the largest logit of row b, ties to the lower trimmed index (the
+ * lower target id), q[b, :] = one-hot at j* (the limit of softmax(z/T)),
+ * token = trim_ids[j*]; uniforms are not read and may be NULL.  T < 0 or
+ * non-finite: VT_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */
 int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                   const uint16_t* W_trim, const int32_t* trim_ids, int32_t K,
@@ -186,7 +191,8 @@ int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
  *  u_accept  f32  [B, gamma]      accept uniforms
  *  u_resample f32 [B, gamma+1]    uniform of the residual (or bonus) draw;
  *                                 entry n_b is used
- *  temperature                    T > 0, the T that produced q
+ *  temperature                    T > 0, the T that produced q; T == 0
+ *                                 verifies greedily (below)
  *  out_tokens int32 [B, gamma+1]  out: draft[0..n_b-1], then the drawn
  *                                 token, then -1
  *  out_num_accepted int32 [B]     out: n_b in [0, gamma]
@@ -196,6 +202,17 @@ int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
  *  dev_status int32 [1]           out: VT_DEV_BAD_DRAFT, VT_DEV_NONFINITE,
  *                                 VT_DEV_ZERO_RESIDUAL, VT_DEV_TIMEOUT
  * 1 <= gamma <= 64, 1 <= B, 1 <= K <= V <= 2^22.
+ *
+ * T == 0, greedy verification ([VT] section 4: a drafted token is accepted
+ * only if it exactly matches the target's choice; Algorithm 2): position i
+ * keeps x_i iff x_i is the largest logit of logits[b, i, :] (ties to the
+ * lower id, compared exactly as given); the first mismatch n is replaced by
+ * that row's choice and the block ends; with no mismatch the choice at
+ * position gamma is appended.  q, inv_map, u_accept and u_resample are not
+ * read (may be NULL; K only sizes the workspace).  out_accept_prob is 1 at
+ * accepted positions, 0 at the rejected one, NaN after.  dev_status:
+ * VT_DEV_BAD_DRAFT (a drafted id outside [0, V) reached by the walk),
+ * VT_DEV_NONFINITE.
  * ---------------------------------------------------------------------- */
 size_t vt_verify_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t K);
 int vt_verify(const void* target_logits, int32_t logits_dtype,

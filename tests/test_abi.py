@@ -64,7 +64,19 @@ def test_host_argument_checks_need_no_gpu(lib):
     fake = ctypes.c_void_p(256)
     st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 5, fake, fake, fake, -1.0,
                        fake, fake, None, fake, fake, 1 << 20, None)
-    assert st == _lib.VT_ERR_INVALID_ARG          # temperature <= 0
+    assert st == _lib.VT_ERR_INVALID_ARG          # temperature < 0
+    st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 5, fake, fake, fake, float("nan"),
+                       fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # temperature not finite
+    st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 5, fake, fake, fake, 1.0,
+                       fake, fake, None, fake, None, 0, None)
+    assert st == _lib.VT_ERR_WORKSPACE            # sampling needs q and uniforms: given
+    st = lib.vt_verify(fake, 0, 1, 1, 10, None, None, 5, fake, None, None, 1.0,
+                       fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # sampling without q / uniforms
+    st = lib.vt_verify(fake, 0, 1, 1, 10, None, None, 5, fake, None, None, 0.0,
+                       fake, fake, None, fake, None, 0, None)
+    assert st == _lib.VT_ERR_WORKSPACE            # greedy: q and uniforms not needed
     st = lib.vt_verify(fake, 0, 1, 1, 10, fake, fake, 11, fake, fake, fake, 1.0,
                        fake, fake, None, fake, fake, 1 << 20, None)
     assert st == _lib.VT_ERR_INVALID_ARG          # K > V
@@ -74,3 +86,20 @@ def test_host_argument_checks_need_no_gpu(lib):
     st = lib.vt_verify(fake, 7, 1, 1, 10, fake, fake, 5, fake, fake, fake, 1.0,
                        fake, fake, None, fake, fake, 1 << 20, None)
     assert st == _lib.VT_ERR_INVALID_ARG          # unknown dtype
+
+
+def test_draft_argument_checks_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    fake = ctypes.c_void_p(256)
+    # vt_draft_logits needs T > 0; vt_draft_step also accepts T == 0 (greedy)
+    st = lib.vt_draft_logits(fake, 2, 8, fake, 16, 0.0, fake, 16, fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG
+    st = lib.vt_draft_step(fake, 2, 8, fake, fake, 16, fake, -1.0, fake, 16, fake, 1, fake,
+                           fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG
+    st = lib.vt_draft_step(fake, 2, 8, fake, fake, 16, None, 1.0, fake, 16, fake, 1, fake,
+                           fake, 1 << 20, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # sampling needs uniforms
+    st = lib.vt_draft_step(fake, 2, 8, fake, fake, 16, None, 0.0, fake, 16, fake, 1, fake,
+                           None, 0, None)
+    assert st == _lib.VT_ERR_WORKSPACE            # greedy: uniforms not needed
