@@ -39,6 +39,10 @@ pages or the mathematics fix (none is "parity unpinned"):
                          the planted naive redraw (tests/test_oracle_verify.py)
 * token_histogram        hand-worked fixtures, collections.Counter, sum = N
 * top_k                  hand-worked ties, Python sorted() on (-count, id)
+* ranking / top_p /      hand-worked counts; brute force over every prefix
+  min_count              length; Top-P at P = 1 keeps every counted id; the
+                         selections agree with top_k at their own K
+                         (tests/test_oracle_select.py)
 * trim_head              bit-for-bit rows, inverse map, head sizes of
                          VocabTrim's Tables 1-3
 * draft_logits           exact rational dot products; one-hot hidden
@@ -56,7 +60,7 @@ pages or the mathematics fix (none is "parity unpinned"):
 """
 from .sampling import inverse_cdf, InverseCdfResult  # noqa: F401
 from .vocabtrim import (token_histogram, top_k, trim_head, bf16_to_f64,  # noqa: F401
-                        draft_logits, draft_step, BadInput)
+                        draft_logits, draft_step, BadInput, ranking, top_p, min_count)
 from .speculative import (softmax, acceptance_probability, residual_weights,  # noqa: F401
                           verify, VerifyResult)
 from .greedy import (argmax_lowest, top2_gap, draft_step_greedy, verify_greedy,  # noqa: F401

@@ -8,6 +8,11 @@ LLMs" (arXiv 2506.22694).
 * ``top_k``            - eq. (1), Top-K(c, k): the k ids with the largest
   counts.  The page does not order ties; the lower id wins (reading fixed for
   the calibration workload), and the result is ranked (count desc, id asc).
+* ``top_p`` / ``min_count`` - section 3 notes the trimmed vocabulary may also
+  be chosen by Top-P or by a minimum frequency in the calibration data; the
+  page defines neither, so: the smallest ranked prefix holding at least a
+  fraction P of the calibration tokens, and every id counted at least f
+  times.
 * ``trim_head``        - eq. (1), W^Trim = W[Top-K(c,k), :], with the rows
   kept in ascending id order (the page fixes no order), plus the token index
   mapper T_{d->t} of Algorithm 2 (trimmed index -> target id, here
@@ -59,6 +64,42 @@ def top_k(counts, K: int) -> np.ndarray:
     # lexsort: last key is primary -> sort by -count, then by id
     order = np.lexsort((ids, -c))
     return order[:K].astype(np.int32)
+
+
+def ranking(counts) -> np.ndarray:
+    """All V ids ranked by (count descending, id ascending)."""
+    c = np.asarray(counts, dtype=np.int64)
+    return top_k(c, c.size)
+
+
+def top_p(counts, P: float):
+    """Top-P selection (section 3: the trimmed vocabulary may be chosen by
+    Top-P instead of Top-K).  Reading: the smallest K such that the K
+    highest-ranked ids cover at least a fraction P of the calibration tokens,
+    sum of their counts >= P * sum(c), compared in fp64.  P in (0, 1]; no
+    calibration tokens gives K = 0.  Returns (ranked ids [V], K)."""
+    P = float(P)
+    if not 0.0 < P <= 1.0:
+        raise ValueError("need 0 < P <= 1")
+    c = np.asarray(counts, dtype=np.int64)
+    order = ranking(c)
+    total = int(c.sum())
+    if total == 0:
+        return order, 0
+    run = 0
+    for k, t in enumerate(order):
+        run += int(c[t])
+        if run >= P * total:
+            return order, k + 1
+    return order, int(np.count_nonzero(c))  # not reached: run ends at total
+
+
+def min_count(counts, f: int):
+    """Minimum-frequency selection (section 3): every id seen at least f
+    times in the calibration stream.  Returns (ranked ids [V], K) with K =
+    #{t : c[t] >= f}; the selected ids are the first K of the ranking."""
+    c = np.asarray(counts, dtype=np.int64)
+    return ranking(c), int(np.count_nonzero(c >= int(f)))
 
 
 def trim_head(W_bits, topk_ids):
