@@ -498,7 +498,8 @@ def main():
         "gpu_launches": sum(KERNELS_PER_CALL[r] * CALLS_PER_STEP[r] for r in ROWS) * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "dev_status": status,
-        "next_rows": {"greedy_block": run_greedy_block(torch, vt, step)},
+        "next_rows": {"greedy_block": run_greedy_block(torch, vt, step),
+                      **run_selection(torch, vt, step)},
     }
 
     if not args.no_e2e:
@@ -553,6 +554,38 @@ def run_greedy_block(torch, vt, step, nblocks: int = 100):
             "achieved_gbs": bytes_block / (us * 1e-6) / 1e9,
             "mean_accepted": float(step.out_n.float().mean().item()), "dev_status": status,
             "note": "temperature 0: greedy drafting and verification, calibrate/trim excluded"}
+
+
+def run_selection(torch, vt, step, ncalls: int = 20):
+    """Top-P (P = 0.95) and minimum-frequency (f = 64) selection on the
+    step's 50M calibration ids: histogram, full ranking and K per call."""
+    out = {}
+    ws = torch.empty(vt.workspace_bytes("select", n=N_CAL, V=V), dtype=torch.uint8,
+                     device=step.ids.device)
+    ranked = torch.empty(V, dtype=torch.int32, device=step.ids.device)
+    k_out = torch.empty(1, dtype=torch.int32, device=step.ids.device)
+    calls = {"top_p_0.95": lambda: vt.vt_calibrate_top_p(
+                 step.ids, V, 0.95, counts=step.counts, ranked_ids=ranked, k_out=k_out,
+                 dev_status=step.status[0:1], workspace=ws),
+             "min_count_64": lambda: vt.vt_calibrate_min_count(
+                 step.ids, V, 64, counts=step.counts, ranked_ids=ranked, k_out=k_out,
+                 dev_status=step.status[0:1], workspace=ws)}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(ncalls):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / ncalls
+        out["calibrate_" + name] = {"us_per_call": us, "K": int(k_out.item()),
+                                    "achieved_gbs": algorithmic_bytes()["calibrate"] / (us * 1e-6) / 1e9,
+                                    "dev_status": int(step.status[0].item())}
+    return out
 
 
 def run_e2e(torch, step, host, stream, args, dist, dev, world):

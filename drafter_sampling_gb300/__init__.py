@@ -17,8 +17,8 @@ from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
                    VT_DEV_ZERO_RESIDUAL, VT_F32,
                    VtError)
 
-__all__ = ["vt_calibrate_topk", "vt_trim_head", "vt_draft_logits", "vt_draft_step",
-           "vt_verify", "workspace_bytes", "VtError", "lib"]
+__all__ = ["vt_calibrate_topk", "vt_calibrate_top_p", "vt_calibrate_min_count", "vt_trim_head",
+           "vt_draft_logits", "vt_draft_step", "vt_verify", "workspace_bytes", "VtError", "lib"]
 
 
 def lib():
@@ -67,6 +67,8 @@ def workspace_bytes(kind: str, **kw) -> int:
     L = lib()
     if kind == "calibrate":
         return L.vt_calibrate_topk_workspace_bytes(kw["n"], kw["V"], kw["K"])
+    if kind == "select":
+        return L.vt_calibrate_select_workspace_bytes(kw["n"], kw["V"])
     if kind == "trim":
         return L.vt_trim_head_workspace_bytes(kw["V"], kw["K"])
     if kind == "draft":
@@ -104,6 +106,51 @@ def vt_calibrate_topk(ids, V: int, K: int, counts=None, topk_ids=None, dev_statu
                              _stream_ptr(stream))
     _lib.check("vt_calibrate_topk", st)
     return counts, topk_ids, dev_status
+
+
+def _calibrate_select(fn: str, ids, V: int, param, counts, ranked_ids, k_out, dev_status,
+                      workspace, stream):
+    torch = _torch()
+    _dev(ids, "ids", (torch.int32,), 1)
+    dev = ids.device
+    n = ids.numel()
+    if counts is None:
+        counts = torch.empty(V, dtype=torch.int32, device=dev)
+    if ranked_ids is None:
+        ranked_ids = torch.empty(V, dtype=torch.int32, device=dev)
+    if k_out is None:
+        k_out = torch.empty(1, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    _dev(counts, "counts", (torch.int32, torch.uint32), 1)
+    _dev(ranked_ids, "ranked_ids", (torch.int32,), 1)
+    if counts.numel() != V or ranked_ids.numel() != V:
+        raise ValueError("counts and ranked_ids must have V elements")
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_calibrate_select_workspace_bytes(n, V), dev)
+    st = getattr(L, fn)(ids.data_ptr(), n, V, param, counts.data_ptr(), ranked_ids.data_ptr(),
+                        k_out.data_ptr(), dev_status.data_ptr(), workspace.data_ptr(),
+                        workspace.numel(), _stream_ptr(stream))
+    _lib.check(fn, st)
+    return counts, ranked_ids, k_out, dev_status
+
+
+def vt_calibrate_top_p(ids, V: int, P: float, counts=None, ranked_ids=None, k_out=None,
+                       dev_status=None, workspace=None, stream=None):
+    """Token histogram, full ranking, and K = the smallest ranked prefix whose
+    counts reach P of the calibration tokens.  Returns (counts [V], ranked_ids
+    [V], k_out int32 [1] on the device, dev_status [1])."""
+    return _calibrate_select("vt_calibrate_top_p", ids, V, float(P), counts, ranked_ids, k_out,
+                             dev_status, workspace, stream)
+
+
+def vt_calibrate_min_count(ids, V: int, min_count: int, counts=None, ranked_ids=None, k_out=None,
+                           dev_status=None, workspace=None, stream=None):
+    """Token histogram, full ranking, and K = the number of ids counted at
+    least min_count times.  Returns (counts, ranked_ids, k_out, dev_status)."""
+    return _calibrate_select("vt_calibrate_min_count", ids, V, int(min_count), counts,
+                             ranked_ids, k_out, dev_status, workspace, stream)
 
 
 def vt_trim_head(W, topk_ids, W_trim=None, trim_ids=None, inv_map=None, dev_status=None,

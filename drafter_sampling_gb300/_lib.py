@@ -42,6 +42,10 @@ SIGNATURES = {
     "vt_abi_version": (C.c_int, []),
     "vt_calibrate_topk_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "vt_calibrate_topk": (C.c_int, [_p, _i64, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
+    "vt_calibrate_select_workspace_bytes": (_sz, [_i64, _i32]),
+    "vt_calibrate_top_p": (C.c_int, [_p, _i64, _i32, C.c_double, _p, _p, _p, _p, _p, _sz, _p]),
+    "vt_calibrate_min_count": (C.c_int, [_p, _i64, _i32, C.c_uint32, _p, _p, _p, _p, _p, _sz,
+                                         _p]),
     "vt_trim_head_workspace_bytes": (_sz, [_i32, _i32]),
     "vt_trim_head": (C.c_int, [_p, _i32, _i32, _p, _i32, _p, _p, _p, _p, _p, _sz, _p]),
     "vt_draft_workspace_bytes": (_sz, [_i32, _i32, _i32]),

@@ -376,6 +376,7 @@ struct SortPassArgs {
   unsigned* keys_out;       // not written by the last pass
   int* vals_out;
   int* topk_ids;            // written by the last pass: ranks < K
+  unsigned* keys_last;      // the last pass also writes the sorted keys here, if not null
   int K;
   int V;
   int shift;
@@ -507,7 +508,10 @@ __global__ void __launch_bounds__(kRsNT, 1) sort_pass_kernel(SortPassArgs a) {
     const unsigned pos = gpos[d] + ((unsigned)j - tstart[d]);
     if (pos >= (unsigned)a.V) continue;  // only after a timed-out wait
     if (a.last) {
-      if (pos < (unsigned)a.K) a.topk_ids[pos] = sval[j];
+      if (pos < (unsigned)a.K) {
+        a.topk_ids[pos] = sval[j];
+        if (a.keys_last != nullptr) a.keys_last[pos] = k;
+      }
     } else {
       a.keys_out[pos] = k;
       a.vals_out[pos] = sval[j];
@@ -904,10 +908,14 @@ extern "C" size_t vt_calibrate_topk_workspace_bytes(int64_t n, int32_t V, int32_
   return vt::carve_calib(nullptr, V, nullptr).bytes;
 }
 
-extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
-                                 uint32_t* counts, int32_t* topk_ids, int32_t* dev_status,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
-  using namespace vt;
+namespace vt {
+namespace {
+// counts, then the K best-ranked ids; with want_keys the last sort pass also
+// leaves the sorted keys (~count, rank order) in the workspace (*keys_out)
+int calibrate_impl(const int32_t* ids, int64_t n, int32_t V, int32_t K, uint32_t* counts,
+                   int32_t* topk_ids, int32_t* dev_status, void* workspace,
+                   size_t workspace_bytes, void* stream, bool want_keys,
+                   const unsigned** keys_out) {
   if (n < 0 || V < 1 || V > (1 << 30) || K < 1 || K > V) return VT_ERR_INVALID_ARG;
   if ((n > 0 && !ids) || !counts || !topk_ids || !dev_status) return VT_ERR_INVALID_ARG;
   if (V > kRsMaxV) return VT_ERR_UNSUPPORTED;
@@ -916,6 +924,9 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
   CalibWs ws = carve_calib(workspace, V, &plan);
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the last pass reads keys[(P) & 1] and writes nothing else: keys[(P - 1) & 1] is free
+  unsigned* keys_last = want_keys ? ws.keys[(plan.passes - 1) & 1] : nullptr;
+  if (keys_out != nullptr) *keys_out = keys_last;
 
   const int64_t nzero = calib_zero_words(V, plan);
   const int64_t zwork = std::max<int64_t>(V, nzero);
@@ -963,6 +974,7 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
     a.keys_out = ws.keys[p & 1];
     a.vals_out = ws.vals[p & 1];
     a.topk_ids = topk_ids;
+    a.keys_last = keys_last;
     a.K = K;
     a.V = V;
     a.shift = p * plan.D;
@@ -988,6 +1000,210 @@ extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32
     VT_RETURN_IF_CUDA(e);
   }
   return VT_OK;
+}
+
+// Top-P / minimum-frequency selection over the sorted keys (~count, rank
+// order).  select_sums: per 1024 ranks, the sum of the counts and how many
+// reach min_count.  select_find: one CTA scans the chunk sums, finds the
+// chunk where the running sum reaches P * total, and scans that chunk.
+constexpr int kSelChunk = 1024;
+
+__global__ void __launch_bounds__(kSelChunk)
+select_sums_kernel(const unsigned* __restrict__ keys, int V, unsigned min_count,
+                   unsigned long long* __restrict__ csum, int* __restrict__ ccnt) {
+  __shared__ unsigned long long ws[kSelChunk / 32];
+  __shared__ int wc[kSelChunk / 32];
+  griddep_wait();  // the sort is complete
+  const int r = blockIdx.x * kSelChunk + threadIdx.x;
+  const unsigned c = (r < V) ? ~keys[r] : 0u;
+  unsigned long long v = c;
+  int k = (r < V && c >= min_count) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, o);
+    k += __shfl_xor_sync(0xffffffffu, k, o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    ws[warp] = v;
+    wc[warp] = k;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+    int n = 0;
+    for (int w = 0; w < kSelChunk / 32; ++w) {
+      t += ws[w];
+      n += wc[w];
+    }
+    csum[blockIdx.x] = t;
+    ccnt[blockIdx.x] = n;
+  }
+}
+
+// inclusive block scan of one u64 per thread (kSelChunk threads)
+__device__ __forceinline__ unsigned long long sel_scan(unsigned long long v,
+                                                       unsigned long long* wsum,
+                                                       unsigned long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  unsigned long long pre = 0, tot = 0;
+  for (int w = 0; w < kSelChunk / 32; ++w) {
+    if (w < warp) pre += wsum[w];
+    tot += wsum[w];
+  }
+  __syncthreads();
+  total = tot;
+  return pre + x;
+}
+
+// mode 0: Top-P; mode 1: minimum count
+__global__ void __launch_bounds__(kSelChunk)
+select_find_kernel(const unsigned* __restrict__ keys, int V, int nchunks, int mode, double P,
+                   const unsigned long long* __restrict__ csum, const int* __restrict__ ccnt,
+                   int* __restrict__ k_out) {
+  __shared__ unsigned long long wsum[kSelChunk / 32];
+  __shared__ int imin[kSelChunk / 32];
+  __shared__ int s_chunk;
+  __shared__ unsigned long long s_base;
+  griddep_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (nchunks + kSelChunk - 1) / kSelChunk;  // chunks per thread, in order
+  const int c0 = tid * per, c1 = min(nchunks, c0 + per);
+  if (mode == 1) {
+    long long n = 0;
+    for (int c = c0; c < c1; ++c) n += ccnt[c];
+    unsigned long long tot;
+    sel_scan((unsigned long long)n, wsum, tot);
+    if (tid == 0) *k_out = (int)tot;
+    return;
+  }
+  unsigned long long mine = 0;
+  for (int c = c0; c < c1; ++c) mine += csum[c];
+  unsigned long long total;
+  const unsigned long long incl = sel_scan(mine, wsum, total);
+  if (total == 0ull) {
+    if (tid == 0) *k_out = 0;
+    return;
+  }
+  const double thr = P * (double)total;
+  // the first chunk whose running sum reaches thr
+  int cand = 0x7fffffff;
+  unsigned long long run = incl - mine;
+  for (int c = c0; c < c1; ++c) {
+    run += csum[c];
+    if ((double)run >= thr) {
+      cand = c;
+      break;
+    }
+  }
+  int m = cand;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) imin[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    int mm = imin[0];
+    for (int w = 1; w < kSelChunk / 32; ++w) mm = min(mm, imin[w]);
+    s_chunk = mm;
+  }
+  __syncthreads();
+  const int cs = s_chunk;
+  // the base of chunk cs, recomputed by the thread that owns it
+  if (cs >= c0 && cs < c1) {
+    unsigned long long b = incl - mine;
+    for (int c = c0; c < cs; ++c) b += csum[c];
+    s_base = b;
+  }
+  __syncthreads();
+  // scan the chunk's counts in rank order
+  const int r = cs * kSelChunk + tid;
+  const unsigned long long cnt = (cs < nchunks && r < V) ? (unsigned long long)(~keys[r]) : 0ull;
+  unsigned long long ctot;
+  const unsigned long long cin = sel_scan(cnt, wsum, ctot) + s_base;
+  const int hit = ((double)cin >= thr && cnt > 0ull) ? tid : 0x7fffffff;
+  m = hit;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) imin[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    int mm = imin[0];
+    for (int w = 1; w < kSelChunk / 32; ++w) mm = min(mm, imin[w]);
+    *k_out = cs * kSelChunk + mm + 1;
+  }
+}
+
+// the calibration workspace followed by the chunk sums and counts
+size_t select_workspace_bytes(int64_t n, int32_t V) {
+  (void)n;
+  if (V < 1 || V > kRsMaxV) return 0;
+  const size_t nchunks = (size_t)(V + kSelChunk - 1) / kSelChunk;
+  return carve_calib(nullptr, V, nullptr).bytes + align_up(nchunks * 8, 256) +
+         align_up(nchunks * 4, 256);
+}
+
+int select_impl(const int32_t* ids, int64_t n, int32_t V, int mode, double P, unsigned min_count,
+                uint32_t* counts, int32_t* ranked_ids, int32_t* k_out, int32_t* dev_status,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!k_out) return VT_ERR_INVALID_ARG;
+  const size_t need = select_workspace_bytes(n, V);
+  if (need == 0) return V > kRsMaxV ? VT_ERR_UNSUPPORTED : VT_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return VT_ERR_WORKSPACE;
+  const unsigned* keys = nullptr;
+  int st = calibrate_impl(ids, n, V, V, counts, ranked_ids, dev_status, workspace, workspace_bytes,
+                          stream, true, &keys);
+  if (st != VT_OK) return st;
+  const SortPlan plan = sort_plan(n, V);
+  const CalibWs ws = carve_calib(workspace, V, &plan);
+  char* extra = static_cast<char*>(workspace) + ws.bytes;
+  const int nchunks = (V + kSelChunk - 1) / kSelChunk;
+  unsigned long long* csum = reinterpret_cast<unsigned long long*>(extra);
+  int* ccnt = reinterpret_cast<int*>(extra + align_up((size_t)nchunks * 8, 256));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  VT_RETURN_IF_CUDA(launch_pdl(select_sums_kernel, dim3((unsigned)nchunks), dim3(kSelChunk), 0, s,
+                               keys, (int)V, min_count, csum, ccnt));
+  VT_RETURN_IF_CUDA(launch_pdl(select_find_kernel, dim3(1), dim3(kSelChunk), 0, s, keys, (int)V,
+                               nchunks, mode, P, (const unsigned long long*)csum,
+                               (const int*)ccnt, k_out));
+  return VT_OK;
+}
+}  // namespace
+}  // namespace vt
+
+extern "C" int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
+                                 uint32_t* counts, int32_t* topk_ids, int32_t* dev_status,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return vt::calibrate_impl(ids, n, V, K, counts, topk_ids, dev_status, workspace,
+                            workspace_bytes, stream, false, nullptr);
+}
+
+extern "C" size_t vt_calibrate_select_workspace_bytes(int64_t n, int32_t V) {
+  return vt::select_workspace_bytes(n, V);
+}
+
+extern "C" int vt_calibrate_top_p(const int32_t* ids, int64_t n, int32_t V, double P,
+                                  uint32_t* counts, int32_t* ranked_ids, int32_t* k_out,
+                                  int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!(P > 0.0 && P <= 1.0)) return VT_ERR_INVALID_ARG;
+  return vt::select_impl(ids, n, V, 0, P, 0u, counts, ranked_ids, k_out, dev_status, workspace,
+                         workspace_bytes, stream);
+}
+
+extern "C" int vt_calibrate_min_count(const int32_t* ids, int64_t n, int32_t V,
+                                      uint32_t min_count, uint32_t* counts, int32_t* ranked_ids,
+                                      int32_t* k_out, int32_t* dev_status, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return vt::select_impl(ids, n, V, 1, 0.0, min_count, counts, ranked_ids, k_out, dev_status,
+                         workspace, workspace_bytes, stream);
 }
 extern "C" size_t vt_trim_head_workspace_bytes(int32_t V, int32_t K) {
   (void)K;

@@ -103,6 +103,38 @@ int vt_calibrate_topk(const int32_t* ids, int64_t n, int32_t V, int32_t K,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Vocabulary selection by Top-P or by a minimum frequency.  [VT] section 3
+ * notes that the trimmed vocabulary may also be chosen by Top-P or by the
+ * minimum frequency of tokens in the calibration data instead of Top-K; the
+ * page defines neither, and these entry points take the plainest readings:
+ *  vt_calibrate_top_p      K = the smallest prefix length of the ranking
+ *                          whose counts reach P * (sum of all counts),
+ *                          compared in fp64; 0 < P <= 1; K = 0 when no id
+ *                          was counted
+ *  vt_calibrate_min_count  K = the number of ids counted at least min_count
+ *                          times (they are the first K of the ranking)
+ *
+ *  ids, n, V      as vt_calibrate_topk (V <= 2^22)
+ *  counts     uint32 [V]   out: c[t]
+ *  ranked_ids int32  [V]   out: all V ids ranked (count desc, id asc)
+ *  k_out      int32  [1]   out, device memory: K.  Read it once the stream
+ *                          has synchronised; ranked_ids[0..K) is the
+ *                          selection, ready for vt_trim_head.
+ *  dev_status int32  [1]   out: VT_DEV_BAD_ID, VT_DEV_TIMEOUT
+ * Workspace: vt_calibrate_select_workspace_bytes(n, V) bytes (0 when V is
+ * out of range).  P outside (0, 1] or non-finite: VT_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+size_t vt_calibrate_select_workspace_bytes(int64_t n, int32_t V);
+int vt_calibrate_top_p(const int32_t* ids, int64_t n, int32_t V, double P,
+                       uint32_t* counts, int32_t* ranked_ids, int32_t* k_out,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                       void* stream);
+int vt_calibrate_min_count(const int32_t* ids, int64_t n, int32_t V, uint32_t min_count,
+                           uint32_t* counts, int32_t* ranked_ids, int32_t* k_out,
+                           int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* ------------------------------------------------------------------------
  * Trimmed LM head.  [VT] eq. (1): W^Trim = W[Top-K(c,k), :]; Algorithm 2's
  * token index mapper T_{d->t} (trimmed index -> target id) and its inverse.
  * Rows are kept in ascending target-id order.

@@ -103,3 +103,18 @@ def test_draft_argument_checks_need_no_gpu(lib):
     st = lib.vt_draft_step(fake, 2, 8, fake, fake, 16, None, 0.0, fake, 16, fake, 1, fake,
                            None, 0, None)
     assert st == _lib.VT_ERR_WORKSPACE            # greedy: uniforms not needed
+
+
+def test_selection_argument_checks_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    fake = ctypes.c_void_p(256)
+    assert lib.vt_calibrate_select_workspace_bytes(1000, 128256) > \
+        lib.vt_calibrate_topk_workspace_bytes(1000, 128256, 10)
+    assert lib.vt_calibrate_select_workspace_bytes(1000, (1 << 22) + 1) == 0
+    for P in (0.0, -0.5, 1.5, float("nan")):
+        st = lib.vt_calibrate_top_p(fake, 10, 100, P, fake, fake, fake, fake, fake, 1 << 24, None)
+        assert st == _lib.VT_ERR_INVALID_ARG, P
+    st = lib.vt_calibrate_top_p(fake, 10, 100, 0.5, fake, fake, None, fake, fake, 1 << 24, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # no k_out
+    st = lib.vt_calibrate_min_count(fake, 10, 100, 3, fake, fake, fake, fake, fake, 16, None)
+    assert st == _lib.VT_ERR_WORKSPACE            # workspace too small
