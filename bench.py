@@ -499,7 +499,8 @@ def main():
         "clocks": clocks.summary(t_wall0, t_wall1),
         "dev_status": status,
         "next_rows": {"greedy_block": run_greedy_block(torch, vt, step),
-                      **run_selection(torch, vt, step)},
+                      **run_selection(torch, vt, step),
+                      "block_graph": run_block_graph(torch, vt, step)},
     }
 
     if not args.no_e2e:
@@ -554,6 +555,48 @@ def run_greedy_block(torch, vt, step, nblocks: int = 100):
             "achieved_gbs": bytes_block / (us * 1e-6) / 1e9,
             "mean_accepted": float(step.out_n.float().mean().item()), "dev_status": status,
             "note": "temperature 0: greedy drafting and verification, calibrate/trim excluded"}
+
+
+def run_block_graph(torch, vt, step, nblocks: int = 100):
+    """The speculative block (six drafting steps + verification, T = 1) as
+    one CUDA graph replayed back to back, beside the same calls launched
+    one by one; tau = mean tokens emitted per block (accepted + 1)."""
+    s = step.vsets[0]
+    g = vt.BlockGraph(step.hidden, step.W_trim, step.trim_ids, step.inv_map, s["logits"],
+                      u_draft=step.u_draft, u_accept=s["u_acc"], u_resample=s["u_res"],
+                      temperature=T)
+
+    def direct():
+        for j in range(GAMMA):
+            vt.vt_draft_step(step.hidden[j], step.W_trim, step.trim_ids, step.u_draft[j], T,
+                             q=step.q[:, j, :], tokens=step.tokens[:, j],
+                             dev_status=step.status[2:3], workspace=step.ws_draft)
+        vt.vt_verify(s["logits"], step.q, step.inv_map, step.tokens, s["u_acc"], s["u_res"], T,
+                     out_tokens=step.out_tokens, out_num_accepted=step.out_n,
+                     out_accept_prob=step.out_acc, dev_status=step.status[3:4],
+                     workspace=step.ws_ver)
+
+    res = {}
+    for name, fn in (("graph", g.launch), ("direct", direct)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(nblocks):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) * 1e3 / nblocks
+    tau = float((g.out_num_accepted.float() + 1).mean().item())
+    status = [int(x) for x in g.dev_status.cpu().tolist()]
+    g.close()
+    return {"value": B * GAMMA / (res["graph"] * 1e-6), "unit": UNIT,
+            "us_per_block_graph": res["graph"], "us_per_block_direct": res["direct"],
+            "tau": tau, "dev_status": status,
+            "note": "drafting steps + verification as one CUDA graph (calibrate/trim excluded); "
+                    "tau = mean tokens per block on the synthetic (unaligned) drafter"}
 
 
 def run_selection(torch, vt, step, ncalls: int = 20):

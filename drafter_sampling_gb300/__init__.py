@@ -18,7 +18,8 @@ from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
                    VtError)
 
 __all__ = ["vt_calibrate_topk", "vt_calibrate_top_p", "vt_calibrate_min_count", "vt_trim_head",
-           "vt_draft_logits", "vt_draft_step", "vt_verify", "workspace_bytes", "VtError", "lib"]
+           "vt_draft_logits", "vt_draft_step", "vt_verify", "BlockGraph", "workspace_bytes",
+           "VtError", "lib"]
 
 
 def lib():
@@ -279,18 +280,24 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
     gamma = R - 1
     if tuple(draft_tokens.shape) != (B, gamma):
         raise ValueError("draft_tokens shape does not match target_logits")
-    given = [x is not None for x in (q, inv_map, u_accept, u_resample)]
-    if not greedy or any(given):
+    # the sampling rule needs all four; the greedy one reads none (any given
+    # one is still checked)
+    if not greedy or q is not None:
         _dev(q, "q", (torch.float32,), 3)
-        _dev(inv_map, "inv_map", (torch.int32,), 1)
-        _dev(u_accept, "u_accept", (torch.float32,), 2)
-        _dev(u_resample, "u_resample", (torch.float32,), 2)
         if tuple(q.shape[:2]) != (B, gamma):
             raise ValueError("q shape does not match target_logits")
-        if tuple(u_accept.shape) != (B, gamma) or tuple(u_resample.shape) != (B, R):
-            raise ValueError("uniform shapes do not match")
+    if not greedy or inv_map is not None:
+        _dev(inv_map, "inv_map", (torch.int32,), 1)
         if inv_map.numel() != V:
             raise ValueError("inv_map must have V entries")
+    if not greedy or u_accept is not None:
+        _dev(u_accept, "u_accept", (torch.float32,), 2)
+        if tuple(u_accept.shape) != (B, gamma):
+            raise ValueError("u_accept must be [B, gamma]")
+    if not greedy or u_resample is not None:
+        _dev(u_resample, "u_resample", (torch.float32,), 2)
+        if tuple(u_resample.shape) != (B, R):
+            raise ValueError("u_resample must be [B, gamma+1]")
     K = q.shape[2] if q is not None else 1
     ptr = lambda x: x.data_ptr() if x is not None else None
     dev = target_logits.device
@@ -313,3 +320,83 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
                      _stream_ptr(stream))
     _lib.check("vt_verify", st)
     return out_tokens, out_num_accepted, out_accept_prob, dev_status
+
+
+class BlockGraph:
+    """One speculative block (gamma drafting steps + verification) captured
+    as a CUDA graph by vt_block_graph_create and replayed by launch().
+
+    The tensors are fixed at capture and kept alive by this object; a replay
+    reads what they hold when it runs.  Outputs (q, draft_tokens,
+    out_tokens, out_num_accepted, out_accept_prob, dev_status [2]) are
+    attributes.  temperature == 0 captures the greedy block (u_draft,
+    u_accept and u_resample may then be None)."""
+
+    def __init__(self, hidden, W_trim, trim_ids, inv_map, target_logits, u_draft=None,
+                 u_accept=None, u_resample=None, temperature: float = 1.0,
+                 want_accept_prob: bool = True):
+        torch = _torch()
+        greedy = float(temperature) == 0.0
+        _dev(hidden, "hidden", _bf16_dtypes(), 3)
+        _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
+        _dev(trim_ids, "trim_ids", (torch.int32,), 1)
+        _dev(inv_map, "inv_map", (torch.int32,), 1)
+        if target_logits.dtype == torch.float32:
+            dt = VT_F32
+        elif target_logits.dtype in _bf16_dtypes():
+            dt = VT_BF16
+        else:
+            raise TypeError("target_logits must be float32 or bf16")
+        _dev(target_logits, "target_logits", (target_logits.dtype,), 3)
+        gamma, B, H = hidden.shape
+        K = W_trim.shape[0]
+        V = target_logits.shape[2]
+        if tuple(target_logits.shape[:2]) != (B, gamma + 1) or inv_map.numel() != V:
+            raise ValueError("target_logits must be [B, gamma+1, V] and inv_map [V]")
+        for name, x, shape in (("u_draft", u_draft, (gamma, B)), ("u_accept", u_accept, (B, gamma)),
+                               ("u_resample", u_resample, (B, gamma + 1))):
+            if x is None:
+                if not greedy:
+                    raise ValueError(f"{name} is needed unless temperature == 0")
+                continue
+            _dev(x, name, (torch.float32,), 2)
+            if tuple(x.shape) != shape:
+                raise ValueError(f"{name} must be {shape}")
+        dev = hidden.device
+        self.q = torch.empty((B, gamma, K), dtype=torch.float32, device=dev)
+        self.draft_tokens = torch.empty((B, gamma), dtype=torch.int32, device=dev)
+        self.out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+        self.out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+        self.out_accept_prob = (torch.empty((B, gamma), dtype=torch.float32, device=dev)
+                                if want_accept_prob else None)
+        self.dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+        L = lib()
+        self.workspace = _ws(L.vt_block_workspace_bytes(B, H, K, V, gamma), dev)
+        self._keep = (hidden, W_trim, trim_ids, inv_map, target_logits, u_draft, u_accept,
+                      u_resample)
+        ptr = lambda x: x.data_ptr() if x is not None else None
+        d = _lib.BlockDesc(B, H, K, V, gamma, dt, float(temperature), ptr(hidden), ptr(W_trim),
+                           ptr(trim_ids), ptr(inv_map), ptr(u_draft), ptr(target_logits),
+                           ptr(u_accept), ptr(u_resample), ptr(self.q), ptr(self.draft_tokens),
+                           ptr(self.out_tokens), ptr(self.out_num_accepted),
+                           ptr(self.out_accept_prob), ptr(self.dev_status),
+                           ptr(self.workspace), self.workspace.numel())
+        import ctypes
+        h = ctypes.c_void_p()
+        _lib.check("vt_block_graph_create", L.vt_block_graph_create(ctypes.byref(d), ctypes.byref(h)))
+        self._handle = h
+
+    def launch(self, stream=None):
+        _lib.check("vt_block_graph_launch",
+                   lib().vt_block_graph_launch(self._handle, _stream_ptr(stream)))
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            lib().vt_block_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -37,6 +37,19 @@ _f32 = C.c_float
 _sz = C.c_size_t
 
 # name -> (restype, argtypes); mirrors include/vt.h
+class BlockDesc(C.Structure):
+    """vt_block_desc of include/vt.h, field for field."""
+    _fields_ = [("B", C.c_int32), ("H", C.c_int32), ("K", C.c_int32), ("V", C.c_int32),
+                ("gamma", C.c_int32), ("logits_dtype", C.c_int32), ("temperature", C.c_float),
+                ("hidden", C.c_void_p), ("W_trim", C.c_void_p), ("trim_ids", C.c_void_p),
+                ("inv_map", C.c_void_p), ("u_draft", C.c_void_p), ("target_logits", C.c_void_p),
+                ("u_accept", C.c_void_p), ("u_resample", C.c_void_p), ("q", C.c_void_p),
+                ("draft_tokens", C.c_void_p), ("out_tokens", C.c_void_p),
+                ("out_num_accepted", C.c_void_p), ("out_accept_prob", C.c_void_p),
+                ("dev_status", C.c_void_p), ("workspace", C.c_void_p),
+                ("workspace_bytes", C.c_size_t)]
+
+
 SIGNATURES = {
     "vt_status_string": (C.c_char_p, [C.c_int]),
     "vt_abi_version": (C.c_int, []),
@@ -57,6 +70,10 @@ SIGNATURES = {
                             _p, _p, _p, _p, _sz, _p]),
     "vt_verify_noalloc": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32,
                                     _p, _p, _p, _p, _p]),
+    "vt_block_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "vt_block_graph_create": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_void_p)]),
+    "vt_block_graph_launch": (C.c_int, [_p, _p]),
+    "vt_block_graph_destroy": (C.c_int, [_p]),
 }
 
 

@@ -35,7 +35,7 @@ def _sources():
 
 
 def _headers():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) +
+    return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
                   glob.glob(os.path.join(HERE, "..", "include", "*.h")))
 
 

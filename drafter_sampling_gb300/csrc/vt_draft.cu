@@ -31,6 +31,7 @@
 #include <cudaTypedefs.h>
 
 #include "vt_common.cuh"
+#include "vt_internal.h"
 #include "vt_umma.cuh"
 
 namespace vt {
@@ -467,18 +468,6 @@ __global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFin
   }
 }
 
-int num_sms() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
-  }
-  return cache[dev];
-}
-
 struct DraftWs {
   float2* part;
   int* status_sink;  // status word of calls that report none (vt_draft_logits)
@@ -702,6 +691,16 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                              const float* uniforms, float temperature, float* q, int64_t ldq,
                              int32_t* tokens, int64_t ld_tokens, int32_t* dev_status,
                              void* workspace, size_t workspace_bytes, void* stream) {
+  return vt::draft_step_impl(hidden, B, H, W_trim, trim_ids, K, uniforms, temperature, q, ldq,
+                             tokens, ld_tokens, dev_status, workspace, workspace_bytes, stream,
+                             1);
+}
+
+int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint16_t* W_trim,
+                        const int32_t* trim_ids, int32_t K, const float* uniforms,
+                        float temperature, float* q, int64_t ldq, int32_t* tokens,
+                        int64_t ld_tokens, int32_t* dev_status, void* workspace,
+                        size_t workspace_bytes, void* stream, int status_reset) {
   using namespace vt;
   int st = check_draft_args(hidden, B, H, W_trim, K, temperature, true);
   if (st != VT_OK) return st;
@@ -714,11 +713,13 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
   if (workspace_bytes < ws.bytes) return VT_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // the projection zeroes the status word (its first CTA runs before the
-  // finalize grid starts: same stream)
+  // with status_reset the projection zeroes the status word (its first CTA
+  // runs before the finalize grid starts: same stream); without, the flags
+  // of this step add to what earlier steps left
   int grid = 0, tile_rows = 0;
   st = launch_head(s, hidden, B, H, W_trim, K, greedy ? 1.0f : VT_LOG2E / temperature, q, ldq,
-                   ws.part, nullptr, 0, dev_status, 1, greedy ? 1 : 0, &grid, &tile_rows);
+                   ws.part, nullptr, 0, dev_status, status_reset, greedy ? 1 : 0, &grid,
+                   &tile_rows);
   if (st != VT_OK) return st;
   if (greedy) {
     GreedyFinArgs ga;

@@ -293,6 +293,63 @@ int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype,
                       int32_t* out_tokens, int32_t* out_num_accepted,
                       float* out_accept_prob, int32_t* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------
+ * One speculative block as a CUDA graph.  [VT] Appendix C.1, Algorithm 2:
+ * draft k (= gamma) tokens through the trimmed head, then score and verify
+ * them.  vt_block_graph_create records gamma vt_draft_step calls (step j
+ * reads hidden[j] and u_draft[j] and writes q[:, j, :] and
+ * draft_tokens[:, j]) followed by one vt_verify call, with the
+ * programmatic-dependent-launch edges between consecutive kernels, into a
+ * CUDA graph on a private stream; vt_block_graph_launch replays the whole
+ * block with one launch on `stream`.  A replay computes exactly what the
+ * same calls made directly would.
+ *
+ * The pointers in the descriptor are fixed at creation: a replay reads
+ * whatever the input buffers hold when it runs and overwrites the outputs.
+ * Layouts (row-major, device memory owned by the caller):
+ *  hidden        bf16 [gamma, B, H]      u_draft  f32 [gamma, B] (NULL if T == 0)
+ *  W_trim        bf16 [K, H]             trim_ids int32 [K], inv_map int32 [V]
+ *  target_logits [B, gamma+1, V] of logits_dtype
+ *  u_accept      f32 [B, gamma], u_resample f32 [B, gamma+1] (NULL if T == 0)
+ *  q             f32 [B, gamma, K] out   draft_tokens int32 [B, gamma] out
+ *  out_tokens    int32 [B, gamma+1] out, out_num_accepted int32 [B] out,
+ *  out_accept_prob f32 [B, gamma] out or NULL
+ *  dev_status    int32 [2] out: [0] the drafting flags of all gamma steps
+ *                (OR), [1] the verification flags
+ *  workspace     vt_block_workspace_bytes(B, H, K, V, gamma) bytes, 256-byte
+ *                aligned, used by every replay (replays on streams without
+ *                an order between them race on it)
+ * The sizes follow vt_draft_step and vt_verify; argument errors of those
+ * calls are returned by vt_block_graph_create (nothing is created then).
+ * *graph receives an opaque handle; vt_block_graph_destroy releases it.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t B, H, K, V, gamma;
+  int32_t logits_dtype;           /* VT_F32 or VT_BF16 */
+  float temperature;              /* T > 0, or 0 for the greedy block */
+  const uint16_t* hidden;
+  const uint16_t* W_trim;
+  const int32_t* trim_ids;
+  const int32_t* inv_map;
+  const float* u_draft;
+  const void* target_logits;
+  const float* u_accept;
+  const float* u_resample;
+  float* q;
+  int32_t* draft_tokens;
+  int32_t* out_tokens;
+  int32_t* out_num_accepted;
+  float* out_accept_prob;
+  int32_t* dev_status;
+  void* workspace;
+  size_t workspace_bytes;
+} vt_block_desc;
+
+size_t vt_block_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t V, int32_t gamma);
+int vt_block_graph_create(const vt_block_desc* desc, void** graph);
+int vt_block_graph_launch(void* graph, void* stream);
+int vt_block_graph_destroy(void* graph);
+
 #ifdef __cplusplus
 }
 #endif

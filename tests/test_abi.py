@@ -118,3 +118,36 @@ def test_selection_argument_checks_need_no_gpu(lib):
     assert st == _lib.VT_ERR_INVALID_ARG          # no k_out
     st = lib.vt_calibrate_min_count(fake, 10, 100, 3, fake, fake, fake, fake, fake, 16, None)
     assert st == _lib.VT_ERR_WORKSPACE            # workspace too small
+
+
+def test_block_descriptor_layout_matches_the_header(tmp_path):
+    # the ctypes mirror of vt_block_desc must have the C layout, field for field
+    import shutil
+    import subprocess
+    from drafter_sampling_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in _lib.BlockDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "vt.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(vt_block_desc));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(vt_block_desc, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(_lib.BlockDesc)
+    assert got[1:] == [getattr(_lib.BlockDesc, f).offset for f in fields]
+
+
+def test_block_graph_argument_checks_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    h = ctypes.c_void_p()
+    assert lib.vt_block_graph_create(None, ctypes.byref(h)) == _lib.VT_ERR_INVALID_ARG
+    d = _lib.BlockDesc()  # all zero: bad sizes
+    assert lib.vt_block_graph_create(ctypes.byref(d), ctypes.byref(h)) == _lib.VT_ERR_INVALID_ARG
+    assert lib.vt_block_graph_launch(None, None) == _lib.VT_ERR_INVALID_ARG
+    assert lib.vt_block_graph_destroy(None) == _lib.VT_OK
+    assert lib.vt_block_workspace_bytes(16, 2048, 32768, 128256, 6) >= \
+        lib.vt_verify_workspace_bytes(16, 6, 128256, 32768)

@@ -1,0 +1,120 @@
+"""The speculative block as a CUDA graph (vt_block_graph_*): a replay gives
+bit-for-bit what the same vt_draft_step / vt_verify calls give when made
+directly (those calls are compared with the oracle in their own tests), it
+reads the input buffers live, and the greedy block works the same way."""
+import numpy as np
+import pytest
+
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import drafter_sampling_gb300 as m
+    from drafter_sampling_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _inputs(B, gamma, H, K, V, seed, dtype="f32"):
+    vi = synthetic.verify_inputs(B=B, gamma=gamma, V=V, K=K, seed=seed, logits_dtype=dtype)
+    g = synthetic.rng(seed, 60)
+    W = synthetic.normal_bf16(g, (K, H), 0.02)
+    hidden = synthetic.hidden_states((gamma, B, H), seed=seed)
+    logits = _dev(vi["logits"].view(np.int16) if dtype == "bf16" else vi["logits"])
+    if dtype == "bf16":
+        logits = logits.view(torch.bfloat16)
+    trim_ids = np.sort(np.flatnonzero(vi["inv_map"] >= 0)).astype(np.int32)
+    return dict(hidden=_dev(hidden.view(np.int16)), W_trim=_dev(W.view(np.int16)),
+                trim_ids=_dev(trim_ids), inv_map=_dev(vi["inv_map"]), logits=logits,
+                u_draft=_dev(synthetic.uniforms(seed, 61, (gamma, B))),
+                u_accept=_dev(vi["u_accept"]), u_resample=_dev(vi["u_resample"]))
+
+
+def _direct(vt, x, T):
+    gamma, B, _ = x["hidden"].shape
+    K = x["W_trim"].shape[0]
+    q = torch.empty((B, gamma, K), dtype=torch.float32, device="cuda")
+    tok = torch.empty((B, gamma), dtype=torch.int32, device="cuda")
+    st_d = torch.zeros(gamma, dtype=torch.int32, device="cuda")
+    for j in range(gamma):
+        vt.vt_draft_step(x["hidden"][j], x["W_trim"], x["trim_ids"],
+                         x["u_draft"][j] if T > 0 else None, T, q=q[:, j, :], tokens=tok[:, j],
+                         dev_status=st_d[j:j + 1])
+    out, n, acc, st_v = vt.vt_verify(x["logits"], q, x["inv_map"], tok,
+                                     x["u_accept"] if T > 0 else None,
+                                     x["u_resample"] if T > 0 else None, T)
+    torch.cuda.synchronize()
+    return q, tok, out, n, acc, int(st_d.max().item()), int(st_v.item())
+
+
+def _graph(vt, x, T):
+    return vt.BlockGraph(x["hidden"], x["W_trim"], x["trim_ids"], x["inv_map"], x["logits"],
+                         u_draft=x["u_draft"] if T > 0 else None,
+                         u_accept=x["u_accept"] if T > 0 else None,
+                         u_resample=x["u_resample"] if T > 0 else None, temperature=T)
+
+
+def _same(a, b):
+    return torch.equal(a, b) if a.dtype != torch.float32 else \
+        torch.equal(a.nan_to_num(-7.0), b.nan_to_num(-7.0))
+
+
+@pytest.mark.parametrize("B,gamma,H,K,V,T,dtype", [
+    (16, 6, 2048, 32768, 128256, 1.0, "f32"),   # the block of the bench step
+    (4, 3, 512, 3000, 20011, 0.7, "bf16"),
+    (8, 4, 256, 2048, 9000, 0.0, "f32"),        # the greedy block
+])
+def test_graph_replay_equals_direct_calls(vt, B, gamma, H, K, V, T, dtype):
+    x = _inputs(B, gamma, H, K, V, seed=B + gamma + V, dtype=dtype)
+    ref = _direct(vt, x, T)
+    g = _graph(vt, x, T)
+    for _ in range(2):                         # replays are repeatable
+        g.launch()
+        torch.cuda.synchronize()
+        got = (g.q, g.draft_tokens, g.out_tokens, g.out_num_accepted, g.out_accept_prob)
+        for a, b in zip(got, ref[:5]):
+            assert _same(a, b)
+        assert int(g.dev_status[0].item()) == ref[5] and int(g.dev_status[1].item()) == ref[6]
+    g.close()
+
+
+def test_graph_reads_inputs_live(vt):
+    x = _inputs(6, 4, 256, 1024, 5000, seed=4)
+    g = _graph(vt, x, 1.0)
+    g.launch()
+    torch.cuda.synchronize()
+    # every accept uniform at 1: every drafted token is rejected at position 0
+    x["u_accept"].fill_(1.0)
+    g.launch()
+    torch.cuda.synchronize()
+    assert (g.out_num_accepted == 0).all()
+    assert (g.out_tokens[:, 1:] == -1).all()
+    # and the graph's result equals a direct run on the changed inputs
+    ref = _direct(vt, x, 1.0)
+    assert torch.equal(g.out_tokens, ref[2])
+    g.close()
+
+
+def test_drafting_flags_of_every_step_are_kept(vt):
+    # a NaN hidden state in step 1 (of 3): the drafting status word keeps its
+    # flag although steps 2 and 3 are clean
+    x = _inputs(4, 3, 256, 1024, 4000, seed=5)
+    h = x["hidden"].clone()
+    h[1, 2, 7] = 0x7fc0
+    x["hidden"] = h
+    g = _graph(vt, x, 1.0)
+    g.launch()
+    torch.cuda.synchronize()
+    assert int(g.dev_status[0].item()) & vt.VT_DEV_NONFINITE
+    g.close()
