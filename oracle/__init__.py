@@ -57,6 +57,13 @@ pages or the mathematics fix (none is "parity unpinned"):
                          tables; equals the stochastic verify at a vanishing
                          temperature for any uniforms; hand-worked blocks
                          (tests/test_oracle_greedy.py)
+* verify_tree_greedy     a chain equals verify_greedy; the deepest accepted
+                         path equals the best root-to-leaf chain (brute
+                         force); lossless tree decoding on the toy tables;
+                         hand-worked trees and depth ties
+* draft_topk             exact integer logits and ties; exp(log q) equals
+                         the pinned draft_step's q; k = 1 is the greedy draft
+                         (tests/test_oracle_tree.py)
 """
 from .sampling import inverse_cdf, InverseCdfResult  # noqa: F401
 from .vocabtrim import (token_histogram, top_k, trim_head, bf16_to_f64,  # noqa: F401
@@ -65,3 +72,4 @@ from .speculative import (softmax, acceptance_probability, residual_weights,  # 
                           verify, VerifyResult)
 from .greedy import (argmax_lowest, top2_gap, draft_step_greedy, verify_greedy,  # noqa: F401
                      GreedyResult)
+from .tree import verify_tree_greedy, draft_topk, TreeResult  # noqa: F401
