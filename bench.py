@@ -127,6 +127,11 @@ class HostInputs:
         self.logits = vi["logits"]
         self.u_accept = vi["u_accept"]
         self.u_resample = vi["u_resample"]
+        # the workload's own drafter distributions and drafts (correlated
+        # with the logits), for the verify-only line and tau
+        self.q_c2 = vi["q"]
+        self.draft_c2 = vi["draft"]
+        self.inv_map_c2 = vi["inv_map"]
 
     def step_inputs(self):
         return dict(ids=self.ids, W=self.W, hidden=self.hidden, u_draft=self.u_draft,
@@ -500,7 +505,9 @@ def main():
         "dev_status": status,
         "next_rows": {"greedy_block": run_greedy_block(torch, vt, step),
                       **run_selection(torch, vt, step),
-                      "block_graph": run_block_graph(torch, vt, step)},
+                      "block_graph": run_block_graph(torch, vt, step),
+                      "verify_c2": run_verify_c2(torch, vt, step, host),
+                      **run_tree(torch, vt, step)},
     }
 
     if not args.no_e2e:
@@ -555,6 +562,92 @@ def run_greedy_block(torch, vt, step, nblocks: int = 100):
             "achieved_gbs": bytes_block / (us * 1e-6) / 1e9,
             "mean_accepted": float(step.out_n.float().mean().item()), "dev_status": status,
             "note": "temperature 0: greedy drafting and verification, calibrate/trim excluded"}
+
+
+def run_tree(torch, vt, step, ncalls: int = 100):
+    """Draft trees of the pages' size (32 nodes) for the step's batch:
+    vt_verify_tree over [B, 33, V] fp32 logits (seeded normal values, one
+    shared random tree shape) and vt_draft_topk (k = 8) through the
+    calibrated trimmed head."""
+    N, k = 32, 8
+    gen = torch.Generator(device=step.dev)
+    gen.manual_seed(5)
+    logits = torch.randn((B, N + 1, V), generator=gen, device=step.dev, dtype=torch.float32)
+    g = np.random.default_rng(5)
+    parent = torch.tensor([-1] + [int(g.integers(-1, i)) for i in range(1, N)],
+                          dtype=torch.int32, device=step.dev)
+    tokens = torch.randint(0, V, (B, N), generator=gen, device=step.dev, dtype=torch.int32)
+    out = torch.empty((B, N + 1), dtype=torch.int32, device=step.dev)
+    n = torch.empty(B, dtype=torch.int32, device=step.dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=step.dev)
+    ws_t = torch.empty(vt.lib().vt_verify_tree_workspace_bytes(B, N, V), dtype=torch.uint8,
+                       device=step.dev)
+    ids = torch.empty((B, k), dtype=torch.int32, device=step.dev)
+    logq = torch.empty((B, k), dtype=torch.float32, device=step.dev)
+    ws_k = torch.empty(vt.lib().vt_draft_topk_workspace_bytes(B, H, K, k), dtype=torch.uint8,
+                       device=step.dev)
+    calls = {
+        "tree_verify_32": (lambda: vt.vt_verify_tree(
+            logits, parent, tokens, out_tokens=out, out_num_accepted=n, out_path=path,
+            dev_status=step.status[3:4], workspace=ws_t), B * (N + 1) * V * 4),
+        "draft_topk_8": (lambda: vt.vt_draft_topk(
+            step.hidden[0], step.W_trim, step.trim_ids, k, T, out_ids=ids, out_logq=logq,
+            dev_status=step.status[2:3], workspace=ws_k), K * H * 2 + 2 * B * K * 4),
+    }
+    res = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(ncalls):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / ncalls
+        res[name] = {"us_per_call": us, "algorithmic_bytes": nbytes,
+                     "achieved_gbs": nbytes / (us * 1e-6) / 1e9}
+    res["tree_verify_32"]["mean_accepted"] = float(n.float().mean().item())
+    del logits
+    return res
+
+
+def run_verify_c2(torch, vt, step, host, ncalls: int = 200):
+    """vt_verify alone on the batched-verify workload's own q and drafts
+    (q = softmax over the trimmed ids of logit + N(0,1), drafts drawn from
+    q): verified positions/s of the verify call and tau = mean tokens per
+    block (accepted + 1)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(step.dev)
+    q, draft, inv_map = t(host.q_c2), t(host.draft_c2), t(host.inv_map_c2)
+
+    def call(k):
+        s = step.vsets[k % step.nsets]
+        vt.vt_verify(s["logits"], q, inv_map, draft, s["u_acc"], s["u_res"], T,
+                     out_tokens=step.out_tokens, out_num_accepted=step.out_n,
+                     out_accept_prob=step.out_acc, dev_status=step.status[3:4],
+                     workspace=step.ws_ver)
+
+    call(0)
+    torch.cuda.synchronize()
+    tau = float((step.out_n.float() + 1).mean().item())
+    status = int(step.status[3].item())
+    for k in range(3):
+        call(k)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(ncalls):
+        call(k)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / ncalls
+    return {"value": B * GAMMA / (us * 1e-6), "unit": UNIT, "us_per_call": us,
+            "achieved_gbs": algorithmic_bytes()["verify"] / (us * 1e-6) / 1e9, "tau": tau,
+            "dev_status": status,
+            "note": "verify only, logits rotating over 2 buffers; tau from the first call"}
 
 
 def run_block_graph(torch, vt, step, nblocks: int = 100):

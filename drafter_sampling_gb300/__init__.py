@@ -18,7 +18,9 @@ from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
                    VtError)
 
 __all__ = ["vt_calibrate_topk", "vt_calibrate_top_p", "vt_calibrate_min_count", "vt_trim_head",
-           "vt_draft_logits", "vt_draft_step", "vt_verify", "BlockGraph", "workspace_bytes",
+           "vt_draft_logits", "vt_draft_step", "vt_draft_topk", "vt_verify", "vt_verify_tree",
+           "BlockGraph",
+           "workspace_bytes",
            "VtError", "lib"]
 
 
@@ -320,6 +322,85 @@ def vt_verify(target_logits, q, inv_map, draft_tokens, u_accept, u_resample,
                      _stream_ptr(stream))
     _lib.check("vt_verify", st)
     return out_tokens, out_num_accepted, out_accept_prob, dev_status
+
+
+def vt_draft_topk(hidden, W_trim, trim_ids, k: int, temperature: float = 1.0, out_ids=None,
+                  out_logq=None, dev_status=None, workspace=None, stream=None):
+    """The drafter's k best trimmed candidates per row (target ids, best
+    first) with log q.  Returns (out_ids int32 [B, k], out_logq [B, k],
+    dev_status [1])."""
+    torch = _torch()
+    _dev(hidden, "hidden", _bf16_dtypes(), 2)
+    _dev(W_trim, "W_trim", _bf16_dtypes(), 2)
+    _dev(trim_ids, "trim_ids", (torch.int32,), 1)
+    B, H = hidden.shape
+    K = W_trim.shape[0]
+    dev = hidden.device
+    if out_ids is None:
+        out_ids = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if out_logq is None:
+        out_logq = torch.empty((B, k), dtype=torch.float32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_draft_topk_workspace_bytes(B, H, K, k), dev)
+    st = L.vt_draft_topk(hidden.data_ptr(), B, H, W_trim.data_ptr(), trim_ids.data_ptr(), K, k,
+                         float(temperature), out_ids.data_ptr(), out_logq.data_ptr(),
+                         dev_status.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                         _stream_ptr(stream))
+    _lib.check("vt_draft_topk", st)
+    return out_ids, out_logq, dev_status
+
+
+def vt_verify_tree(target_logits, parent, tokens, temperature: float = 0.0, out_tokens=None,
+                   out_num_accepted=None, out_path=None, dev_status=None, workspace=None,
+                   stream=None, want_path: bool = True):
+    """Greedy verification of draft trees: target_logits [B, N+1, V] (row 0
+    after the context, row i+1 after node i), parent int32 [B, N] or [N]
+    (shared tree; -1 = the context), tokens int32 [B, N].  Returns
+    (out_tokens [B, N+1], out_num_accepted [B], out_path [B, N] or None,
+    dev_status [1])."""
+    torch = _torch()
+    if target_logits.dtype == torch.float32:
+        dt = VT_F32
+    elif target_logits.dtype in _bf16_dtypes():
+        dt = VT_BF16
+    else:
+        raise TypeError("target_logits must be float32 or bf16")
+    _dev(target_logits, "target_logits", (target_logits.dtype,), 3)
+    _dev(tokens, "tokens", (torch.int32,), 2)
+    _dev(parent, "parent", (torch.int32,), None)
+    B, R, V = target_logits.shape
+    N = R - 1
+    if tuple(tokens.shape) != (B, N):
+        raise ValueError("tokens must be [B, N] with N + 1 = target_logits.shape[1]")
+    if parent.dim() == 1 and parent.numel() == N:
+        pstride = 0
+    elif parent.dim() == 2 and tuple(parent.shape) == (B, N):
+        pstride = N
+    else:
+        raise ValueError("parent must be [N] or [B, N]")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, R), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_path is None and want_path:
+        out_path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(1, dtype=torch.int32, device=dev)
+    L = lib()
+    if workspace is None:
+        workspace = _ws(L.vt_verify_tree_workspace_bytes(B, N, V), dev)
+    st = L.vt_verify_tree(target_logits.data_ptr(), dt, B, N, V, parent.data_ptr(), pstride,
+                          tokens.data_ptr(), float(temperature), out_tokens.data_ptr(),
+                          out_num_accepted.data_ptr(),
+                          out_path.data_ptr() if out_path is not None else None,
+                          dev_status.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          _stream_ptr(stream))
+    _lib.check("vt_verify_tree", st)
+    return out_tokens, out_num_accepted, out_path, dev_status
 
 
 class BlockGraph:

@@ -65,11 +65,17 @@ SIGNATURES = {
     "vt_draft_logits": (C.c_int, [_p, _i32, _i32, _p, _i32, _f32, _p, _i64, _p, _sz, _p]),
     "vt_draft_step": (C.c_int, [_p, _i32, _i32, _p, _p, _i32, _p, _f32, _p, _i64, _p, _i64,
                                 _p, _p, _sz, _p]),
+    "vt_draft_topk_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "vt_draft_topk": (C.c_int, [_p, _i32, _i32, _p, _p, _i32, _i32, _f32, _p, _p, _p, _p, _sz,
+                                _p]),
     "vt_verify_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "vt_verify": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32, _p,
                             _p, _p, _p, _p, _sz, _p]),
     "vt_verify_noalloc": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _p, _i32, _p, _p, _p, _f32,
                                     _p, _p, _p, _p, _p]),
+    "vt_verify_tree_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "vt_verify_tree": (C.c_int, [_p, _i32, _i32, _i32, _i32, _p, _i64, _p, _f32, _p, _p, _p, _p,
+                                 _p, _sz, _p]),
     "vt_block_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "vt_block_graph_create": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_void_p)]),
     "vt_block_graph_launch": (C.c_int, [_p, _p]),

@@ -468,6 +468,145 @@ __global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFin
   }
 }
 
+// ------------------------------------------------------ drafter top-k
+// The drafter's k best trimmed candidates at one position (the expansion
+// step of a draft tree, VocabTrim section 4.1): the k highest z, ties to the
+// lower trimmed index, with log q = log softmax(z / T).  The projection
+// writes z2 = z * log2(e) / T and the per-tile softmax partials; each CTA of
+// topk_chunk takes 1024 ids and leaves its k best in order; topk_final
+// merges the chunks' lists of a row and converts to log q.
+constexpr int kTopkMax = 32;
+constexpr int kTopkChunk = 1024;
+
+struct TopkArgs {
+  const float* z2;       // [B][K]
+  int B, K, k;
+  const float2* part;    // [G][B]
+  int G;
+  float2* cand;          // [B][nchunk][k]: (z2, index), -inf / INT_MAX padding
+  int nchunk;
+  const int* trim_ids;
+  int* out_ids;          // [B][k]
+  float* out_logq;       // [B][k]
+  int* dev_status;
+};
+
+// warp-wide: the best (value, index) over the lanes' heads; returns the lane
+__device__ __forceinline__ int warp_best_lane(float v, int i) {
+  float bv = v;
+  int bi = i, bl = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int wi = __shfl_xor_sync(0xffffffffu, bi, o);
+    const int wl = __shfl_xor_sync(0xffffffffu, bl, o);
+    if (umma::argmax_better(bv, bi, w, wi)) {
+      bv = w;
+      bi = wi;
+      bl = wl;
+    }
+  }
+  return bl;
+}
+
+__global__ void __launch_bounds__(256) topk_chunk_kernel(TopkArgs a) {
+  __shared__ float sv[8][kTopkMax];
+  __shared__ int si[8][kTopkMax];
+  const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_wait();  // the projection has completed
+  // this thread's 4 ids, sorted best first
+  float v[4];
+  int ix[4];
+  const int64_t j0 = (int64_t)c * kTopkChunk + 4 * tid;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int64_t j = j0 + e;
+    v[e] = (j < a.K) ? a.z2[(int64_t)b * a.K + j] : -INFINITY;
+    if (v[e] != v[e]) v[e] = -INFINITY;  // non-finite rows are flagged from the partials
+    ix[e] = (j < a.K) ? (int)j : 0x7fffffff;
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int q = 0; q < 3 - p; ++q)
+      if (umma::argmax_better(v[q], ix[q], v[q + 1], ix[q + 1])) {
+        const float tv = v[q]; v[q] = v[q + 1]; v[q + 1] = tv;
+        const int ti = ix[q]; ix[q] = ix[q + 1]; ix[q + 1] = ti;
+      }
+  // the warp's k best: k rounds over the lanes' heads
+  int head = 0;
+  for (int r = 0; r < a.k; ++r) {
+    const float hv = head < 4 ? v[head] : -INFINITY;
+    const int hi = head < 4 ? ix[head] : 0x7fffffff;
+    const int wl = warp_best_lane(hv, hi);
+    const float bv = __shfl_sync(0xffffffffu, hv, wl);
+    const int bi = __shfl_sync(0xffffffffu, hi, wl);
+    if (lane == 0) {
+      sv[warp][r] = bv;
+      si[warp][r] = bi;
+    }
+    if (lane == wl) ++head;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // merge the 8 warps' lists: lane l < 8 walks list l
+    int h = 0;
+    for (int r = 0; r < a.k; ++r) {
+      const float hv = (lane < 8 && h < a.k) ? sv[lane][h] : -INFINITY;
+      const int hi = (lane < 8 && h < a.k) ? si[lane][h] : 0x7fffffff;
+      const int wl = warp_best_lane(hv, hi);
+      const float bv = __shfl_sync(0xffffffffu, hv, wl);
+      const int bi = __shfl_sync(0xffffffffu, hi, wl);
+      if (lane == 0)
+        a.cand[((int64_t)b * a.nchunk + c) * a.k + r] = make_float2(bv, __int_as_float(bi));
+      if (lane == wl) ++h;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(32) topk_final_kernel(TopkArgs a) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  griddep_wait();
+  // the row's softmax normaliser from the projection's tile partials
+  MS g{kNegBig, 0.f};
+  for (int t = lane; t < a.G; t += 32) {
+    const float2 p = a.part[(int64_t)t * a.B + b];
+    g = ms_combine(g, MS{p.x, p.y});
+  }
+  g = warp_ms_reduce(g);
+  const bool ok = g.s > 0.f && isfinite(g.s) && isfinite(g.m);
+  // lane l walks the chunk lists l, l + 32, ...; each round takes the best head
+  int head[32];  // a.nchunk <= 1024 (host check)
+  const int per = (a.nchunk + 31) / 32;
+  for (int q = 0; q < per; ++q) head[q] = 0;
+  for (int r = 0; r < a.k; ++r) {
+    float hv = -INFINITY;
+    int hi = 0x7fffffff, hq = -1;
+    for (int q = 0; q < per; ++q) {
+      const int c = lane + 32 * q;
+      if (c >= a.nchunk || head[q] >= a.k) continue;
+      const float2 e = a.cand[((int64_t)b * a.nchunk + c) * a.k + head[q]];
+      if (umma::argmax_better(hv, hi, e.x, __float_as_int(e.y))) {
+        hv = e.x;
+        hi = __float_as_int(e.y);
+        hq = q;
+      }
+    }
+    const int wl = warp_best_lane(hv, hi);
+    const float bv = __shfl_sync(0xffffffffu, hv, wl);
+    const int bi = __shfl_sync(0xffffffffu, hi, wl);
+    if (lane == wl && hq >= 0) ++head[hq];
+    if (lane == 0) {
+      const bool have = ok && bi >= 0 && bi < a.K;
+      a.out_ids[(int64_t)b * a.k + r] = have ? a.trim_ids[bi] : -1;
+      // log q = (z2 - m) ln 2 - ln S
+      a.out_logq[(int64_t)b * a.k + r] =
+          have ? (bv - g.m) * 0.6931471805599453f - logf(g.s) : __int_as_float(0x7fc00000);
+    }
+  }
+  if (lane == 0 && !ok) atomicOr(a.dev_status, VT_DEV_NONFINITE);
+}
+
 struct DraftWs {
   float2* part;
   int* status_sink;  // status word of calls that report none (vt_draft_logits)
@@ -772,5 +911,64 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, draft_finalize_kernel, fa));
+  return VT_OK;
+}
+
+extern "C" size_t vt_draft_topk_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t k) {
+  if (B < 1 || K < 1 || k < 1 || k > vt::kTopkMax || k > K) return 0;
+  const size_t nchunk = (size_t)(K + vt::kTopkChunk - 1) / vt::kTopkChunk;
+  return vt::align_up(vt_draft_workspace_bytes(B, H, K), 256) +
+         vt::align_up((size_t)B * K * 4, 256) + vt::align_up((size_t)B * nchunk * k * 8, 256);
+}
+
+extern "C" int vt_draft_topk(const uint16_t* hidden, int32_t B, int32_t H, const uint16_t* W_trim,
+                             const int32_t* trim_ids, int32_t K, int32_t k, float temperature,
+                             int32_t* out_ids, float* out_logq, int32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace vt;
+  int st = check_draft_args(hidden, B, H, W_trim, K, temperature, false);
+  if (st != VT_OK) return st;
+  if (!trim_ids || !out_ids || !out_logq || !dev_status || k < 1 || k > kTopkMax || k > K)
+    return VT_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
+  if (workspace_bytes < vt_draft_topk_workspace_bytes(B, H, K, k)) return VT_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  DraftWs dws = carve_draft(ws, B, K);
+  const size_t off_z = align_up(vt_draft_workspace_bytes(B, H, K), 256);
+  float* z2 = reinterpret_cast<float*>(ws + off_z);
+  const int nchunk = (K + kTopkChunk - 1) / kTopkChunk;
+  if (nchunk > 32 * 32) return VT_ERR_UNSUPPORTED;  // K > 2^20
+  float2* cand = reinterpret_cast<float2*>(ws + off_z + align_up((size_t)B * K * 4, 256));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int grid = 0, tile_rows = 0;
+  st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, z2, K, dws.part, nullptr,
+                   0, dev_status, 1, 0, &grid, &tile_rows);
+  if (st != VT_OK) return st;
+  TopkArgs a;
+  a.z2 = z2;
+  a.B = B;
+  a.K = K;
+  a.k = k;
+  a.part = dws.part;
+  a.G = grid;
+  a.cand = cand;
+  a.nchunk = nchunk;
+  a.trim_ids = trim_ids;
+  a.out_ids = out_ids;
+  a.out_logq = out_logq;
+  a.dev_status = dev_status;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.stream = s;
+  cfg.gridDim = dim3((unsigned)B, (unsigned)nchunk);
+  cfg.blockDim = dim3(256);
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, topk_chunk_kernel, a));
+  cfg.gridDim = dim3((unsigned)B);
+  cfg.blockDim = dim3(32);
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, topk_final_kernel, a));
   return VT_OK;
 }

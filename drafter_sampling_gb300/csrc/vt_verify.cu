@@ -674,11 +674,124 @@ __global__ void __launch_bounds__(kNT) verify_greedy_finish_kernel(VArgs a) {
   }
 }
 
+// ------------------------------------------------------------ draft trees
+// Greedy verification of a draft tree (VocabTrim section 4.1's EAGLE-2
+// trees with the greedy target of section 4): N nodes in topological order,
+// node i with a target id and a parent in {-1} or [0, i) (-1: the context);
+// the target scores N + 1 rows (row 0 after the context, row i + 1 after
+// node i).  Node i is accepted iff its parent is and its token is the
+// target's choice at the parent's row; the block is the path to the
+// deepest accepted node (ties to the lower node) and the choice there.
+constexpr int kMaxTreeNodes = 255;
+
+struct TreeArgs {
+  const int* parent;    // [B][N], or one shared [N] when pstride == 0
+  int64_t pstride;
+  const int* tokens;    // [B][N]
+  int N;
+  int* out_path;        // [B][N] or nullptr
+};
+
+__global__ void __launch_bounds__(kNT) verify_tree_finish_kernel(VArgs a, TreeArgs t) {
+  __shared__ int choice[kMaxTreeNodes + 1];
+  __shared__ unsigned char acc[kMaxTreeNodes];
+  __shared__ unsigned char dep[kMaxTreeNodes];
+  __shared__ int path[kMaxTreeNodes];
+  __shared__ int s_best, s_len, s_flags;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.R, N = t.N;
+  griddep_wait();  // the stats kernel has completed
+  for (int i = warp; i < R; i += kNT / 32) {
+    float v = -INFINITY;
+    int idx = 0x7fffffff;
+    const float2* pp = a.part + ((int64_t)b * R + i) * a.C1;
+    for (int k = lane; k < a.C1; k += 32) {
+      const float2 q = pp[k];
+      if (gbetter(v, idx, q.x, __float_as_int(q.y))) {
+        v = q.x;
+        idx = __float_as_int(q.y);
+      }
+    }
+    warp_gmax(v, idx);
+    if (lane == 0) choice[i] = (v == v && idx >= 0 && (int64_t)idx < a.V) ? idx : -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // nodes in topological order: a parent's verdict is known before its children's
+    int flags = 0, best = -1, best_depth = 0;
+    for (int r = 0; r < R; ++r)
+      if (choice[r] < 0) flags |= VT_DEV_NONFINITE;
+    const int* par = t.parent + (int64_t)b * t.pstride;
+    const int* tok = t.tokens + (int64_t)b * N;
+    for (int i = 0; i < N && !flags; ++i) {
+      const int p = par[i];
+      const int x = tok[i];
+      if (p < -1 || p >= i || x < 0 || (int64_t)x >= a.V) {
+        flags |= VT_DEV_BAD_DRAFT;
+        break;
+      }
+      const bool ok = (p < 0 || acc[p]) && x == choice[p + 1];
+      acc[i] = ok ? 1 : 0;
+      dep[i] = (unsigned char)(p < 0 ? 1 : dep[p] + 1);
+      if (ok && dep[i] > best_depth) {
+        best = i;
+        best_depth = dep[i];
+      }
+    }
+    int len = 0;
+    if (!flags) {
+      for (int i = best; i >= 0; i = par[i]) path[len++] = i;
+      for (int k = 0; k < len / 2; ++k) {  // root first
+        const int tmp = path[k];
+        path[k] = path[len - 1 - k];
+        path[len - 1 - k] = tmp;
+      }
+    }
+    s_best = best;
+    s_len = len;
+    s_flags = flags;
+  }
+  __syncthreads();
+  const int flags = s_flags, len = s_len, best = s_best;
+  for (int i = tid; i < R; i += kNT) {
+    int v = -1;
+    if (!flags) {
+      if (i < len) v = t.tokens[(int64_t)b * N + path[i]];
+      else if (i == len) v = choice[best + 1];
+    }
+    a.out_tokens[(int64_t)b * R + i] = v;
+  }
+  if (t.out_path != nullptr)
+    for (int i = tid; i < N; i += kNT)
+      t.out_path[(int64_t)b * N + i] = (!flags && i < len) ? path[i] : -1;
+  if (tid == 0) {
+    a.out_n[b] = flags ? 0 : len;
+    if (flags) atomicOr(a.dev_status, flags);
+  }
+}
+
 template <typename T>
 int launch_verify_greedy(const VArgs& a, cudaStream_t s) {
   VT_RETURN_IF_CUDA(launch_pdl(verify_greedy_stats_kernel<T>,
                                dim3((unsigned)((int64_t)a.B * a.R), (unsigned)a.C1), s, a));
   VT_RETURN_IF_CUDA(launch_pdl(verify_greedy_finish_kernel, dim3((unsigned)a.B), s, a));
+  return VT_OK;
+}
+
+template <typename T>
+int launch_verify_tree(const VArgs& a, const TreeArgs& t, cudaStream_t s) {
+  VT_RETURN_IF_CUDA(launch_pdl(verify_greedy_stats_kernel<T>,
+                               dim3((unsigned)((int64_t)a.B * a.R), (unsigned)a.C1), s, a));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.B);
+  cfg.blockDim = dim3(kNT);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, verify_tree_finish_kernel, a, t));
   return VT_OK;
 }
 
@@ -819,4 +932,59 @@ extern "C" int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype
   return vt_verify(target_logits, logits_dtype, B, gamma, V, q, inv_map, K, draft_tokens,
                    u_accept, u_resample, temperature, out_tokens, out_num_accepted,
                    out_accept_prob, dev_status, scratch, VT_VERIFY_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" size_t vt_verify_tree_workspace_bytes(int32_t B, int32_t N, int32_t V) {
+  if (B < 1 || N < 1 || N > vt::kMaxTreeNodes || V < 1) return 0;
+  return vt_verify_workspace_bytes(B, N, V, 1);
+}
+
+extern "C" int vt_verify_tree(const void* target_logits, int32_t logits_dtype, int32_t B,
+                              int32_t N, int32_t V, const int32_t* parent, int64_t parent_stride,
+                              const int32_t* tokens, float temperature, int32_t* out_tokens,
+                              int32_t* out_num_accepted, int32_t* out_path, int32_t* dev_status,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace vt;
+  if (!target_logits || !parent || !tokens || !out_tokens || !out_num_accepted || !dev_status)
+    return VT_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kMaxTreeNodes || V < 1 || V > (1 << 22))
+    return VT_ERR_INVALID_ARG;
+  if (parent_stride != 0 && parent_stride < N) return VT_ERR_INVALID_ARG;
+  if (logits_dtype != VT_F32 && logits_dtype != VT_BF16) return VT_ERR_INVALID_ARG;
+  if (!std::isfinite(temperature) || temperature < 0.f) return VT_ERR_INVALID_ARG;
+  if (temperature != 0.f) return VT_ERR_UNSUPPORTED;  // trees are verified greedily
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
+  const VerifyLayout L = verify_layout(B, N, V);
+  if (workspace_bytes < L.bytes) return VT_ERR_WORKSPACE;
+  const size_t esize = (logits_dtype == VT_F32) ? 4 : 2;
+  const int vec = (logits_dtype == VT_F32) ? 4 : 8;
+  VArgs a = {};
+  a.logits = target_logits;
+  a.V = V;
+  a.B = B;
+  a.gamma = N;
+  a.R = N + 1;
+  a.K = 1;
+  a.scale = 1.f;
+  int64_t len1 = std::max<int64_t>(kStatsBytes / (int64_t)esize,
+                                   ((int64_t)V + kMaxChunks1 - 1) / kMaxChunks1);
+  len1 = (len1 + vec - 1) / vec * vec;
+  a.len1 = len1;
+  a.C1 = (int)(((int64_t)V + len1 - 1) / len1);
+  a.C2 = chunks2(V);
+  a.vec_ok = ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
+             (((int64_t)V * esize) % 16 == 0);
+  a.part = reinterpret_cast<float2*>(static_cast<char*>(workspace) + L.part);
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.dev_status = dev_status;
+  TreeArgs t;
+  t.parent = parent;
+  t.pstride = parent_stride;
+  t.tokens = tokens;
+  t.N = N;
+  t.out_path = out_path;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (logits_dtype == VT_F32) return launch_verify_tree<float>(a, t, s);
+  return launch_verify_tree<uint16_t>(a, t, s);
 }

@@ -204,6 +204,26 @@ int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                   void* stream);
 
 /* ------------------------------------------------------------------------
+ * The drafter's top-k candidates at one position: the expansion step of a
+ * draft tree ([VT] section 4.1 grows EAGLE-2 trees with top-K 8 through the
+ * trimmed head).  z as in vt_draft_logits; the k highest z of row b, ties
+ * to the lower trimmed index, best first, mapped to target ids, each with
+ * log q = log softmax(z / T) over the trimmed vocabulary.  How a tree is
+ * grown from them (which nodes to expand, re-ranking) is the caller's.
+ *
+ *  out_ids  int32 [B, k]  out: target ids (-1 for a row with non-finite z)
+ *  out_logq f32   [B, k]  out: log q of each (NaN for such a row)
+ *  dev_status int32 [1]   out: VT_DEV_NONFINITE
+ * 1 <= k <= 32, k <= K <= 2^20; T finite and > 0.  Workspace:
+ * vt_draft_topk_workspace_bytes(B, H, K, k) bytes.
+ * ---------------------------------------------------------------------- */
+size_t vt_draft_topk_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t k);
+int vt_draft_topk(const uint16_t* hidden, int32_t B, int32_t H, const uint16_t* W_trim,
+                  const int32_t* trim_ids, int32_t K, int32_t k, float temperature,
+                  int32_t* out_ids, float* out_logq, int32_t* dev_status,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Batched block verification by modified rejection sampling.
  * [GL] "Why a rejection needs a special draw": accept a drafted x with
  * probability a(x) = min(1, p(x)/q(x)); on rejection draw from
@@ -292,6 +312,44 @@ int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype,
                       const float* u_resample, float temperature,
                       int32_t* out_tokens, int32_t* out_num_accepted,
                       float* out_accept_prob, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Greedy verification of draft trees.  [VT] section 4.1 drafts, builds and
+ * verifies trees as EAGLE-2 does (depth 3, top-K 8, at most 32 tokens) with
+ * the greedy target of section 4; Algorithm 2 keeps the consistent prefix
+ * and replaces the first inconsistent token.  A tree holds N drafted nodes
+ * in topological order: node i carries tokens[b, i] (a target id) and
+ * parent[b, i] in {-1} or [0, i), -1 meaning the context.  The target has
+ * scored N + 1 positions: row 0 after the context, row i + 1 after node i
+ * (with the tree attention of the caller's target model).
+ * Node i is accepted iff its parent is (the context always is) and its
+ * token is the largest logit of its parent's row (ties to the lower id,
+ * compared exactly as given).  The block is the token path from the context
+ * to the deepest accepted node (ties to the lower node index) followed by
+ * the target's choice at that node's row; a chain (parent[i] = i - 1) gives
+ * exactly vt_verify's greedy block.
+ *
+ *  target_logits [B, N+1, V] of logits_dtype
+ *  parent    int32 [B, N]   (row stride parent_stride >= N, or 0: one tree
+ *                            shared by all sequences)
+ *  tokens    int32 [B, N]   drafted target ids
+ *  temperature              0 (greedy); T > 0 returns VT_ERR_UNSUPPORTED
+ *  out_tokens int32 [B, N+1] out: the path's tokens, the target's choice,
+ *                            then -1
+ *  out_num_accepted int32 [B] out: the path length (accepted tokens)
+ *  out_path  int32 [B, N]   out, may be NULL: the path's node indices, -1 after
+ *  dev_status int32 [1]     out: VT_DEV_BAD_DRAFT (a token outside [0, V) or
+ *                            a parent not before its node; that sequence
+ *                            gets -1 tokens), VT_DEV_NONFINITE
+ * 1 <= N <= 255, 1 <= B, V <= 2^22.  Workspace:
+ * vt_verify_tree_workspace_bytes(B, N, V) bytes.
+ * ---------------------------------------------------------------------- */
+size_t vt_verify_tree_workspace_bytes(int32_t B, int32_t N, int32_t V);
+int vt_verify_tree(const void* target_logits, int32_t logits_dtype, int32_t B, int32_t N,
+                   int32_t V, const int32_t* parent, int64_t parent_stride,
+                   const int32_t* tokens, float temperature, int32_t* out_tokens,
+                   int32_t* out_num_accepted, int32_t* out_path, int32_t* dev_status,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * One speculative block as a CUDA graph.  [VT] Appendix C.1, Algorithm 2:
