@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   __shared__ int ired[kFinNT / 32];
   __shared__ int s_tile, s_last;
   __shared__ float s_before;
+  constexpr int kRegTiles = 4;  // tile partials a thread keeps in registers
   const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31;
   float* qrow = a.q + (int64_t)b * a.ldq;
@@ -278,9 +279,11 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   }
   const int per = (a.G + kFinNT - 1) / kFinNT;
   const int t0 = tid * per, t1 = min(a.G, t0 + per);
+  float2 pt[kRegTiles];
   MS mine{kNegBig, 0.f};
   for (int t = t0; t < t1; ++t) {
     const float2 p = a.part[(int64_t)t * a.B + b];
+    if (t - t0 < kRegTiles) pt[t - t0] = p;
     mine = ms_combine(mine, MS{p.x, p.y});
   }
   const MS g = block_ms_reduce<kFinNT>(mine, mred);
@@ -292,25 +295,19 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     return;
   }
   const float m = g.m, invS = 1.f / g.s;
-
-  // normalise this chunk in place
   float w[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) w[e] = (j + e < a.K) ? exp2_approx(z[e] - m) : 0.f;
-  if (a.vec_ok && j + 3 < a.K) {
-    *reinterpret_cast<float4*>(qrow + j) =
-        make_float4(w[0] * invS, w[1] * invS, w[2] * invS, w[3] * invS);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j + e < a.K) qrow[j + e] = w[e] * invS;
-  }
+  auto tile_part = [&](int t) -> float2 {
+    return (t - t0 < kRegTiles) ? pt[t - t0] : a.part[(int64_t)t * a.B + b];
+  };
 
-  // tile holding the draw: scan of tile masses in tile order
+  // tile holding the draw: scan of tile masses in tile order (the token is
+  // chosen before this chunk of q is normalised)
   const float target = a.u[b] * g.s;
   float mass = 0.f;
   for (int t = t0; t < t1; ++t) {
-    const float2 p = a.part[(int64_t)t * a.B + b];
+    const float2 p = tile_part(t);
     mass += p.y * exp2_approx(p.x - m);
   }
   float excl, tot;
@@ -328,7 +325,7 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     float run = excl;
     int last_t = -1;
     for (int t = t0; t < t1; ++t) {
-      const float2 p = a.part[(int64_t)t * a.B + b];
+      const float2 p = tile_part(t);
       const float mt = p.y * exp2_approx(p.x - m);
       if (mt > 0.f) last_t = t;
       if (run + mt > target) {
@@ -354,52 +351,62 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
       if (a.part[(int64_t)t * a.B + b].y > 0.f) tsel = t;
     force_last = true;
   }
-  if (tsel < 0) return;
-  const int64_t r0 = (int64_t)tsel * a.tile_rows;
-  if (r0 < (int64_t)c * kFinChunk || r0 >= (int64_t)(c + 1) * kFinChunk) return;
-
-  // this CTA holds the tile: its rows are consecutive threads of one warp
-  const int64_t r1 = min((int64_t)a.K, r0 + a.tile_rows);
-  const int owner_warp = (int)((r0 - (int64_t)c * kFinChunk) / 4) >> 5;
-  if ((tid >> 5) != owner_warp) return;
-  float v = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e)
-    if (j + e >= r0 && j + e < r1) v += w[e];
-  float x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  const float local = target - before;
-  const unsigned hit = force_last ? 0u : __ballot_sync(0xffffffffu, x > local);
-  int pick = -1;
-  if (hit) {
-    const int l = __ffs(hit) - 1;
-    if (lane == l) {
-      float acc = x - v;
-      int lastp = -1;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (j + e < r0 || j + e >= r1) continue;
-        if (w[e] > 0.f) lastp = (int)(j + e);
-        acc += w[e];
-        if (pick < 0 && acc > local) pick = (int)(j + e);
-      }
-      if (pick < 0) pick = lastp;
-    }
-    pick = __shfl_sync(0xffffffffu, pick, l);
-  } else {
-    // last row with weight in the tile
-    int lp = -1;
+  const int64_t r0 = (int64_t)max(tsel, 0) * a.tile_rows;
+  const bool owner_cta =
+      tsel >= 0 && r0 >= (int64_t)c * kFinChunk && r0 < (int64_t)(c + 1) * kFinChunk;
+  const int owner_warp = owner_cta ? (int)((r0 - (int64_t)c * kFinChunk) / 4) >> 5 : -1;
+  if ((tid >> 5) == owner_warp) {
+    // this CTA holds the tile: its rows are consecutive threads of one warp
+    const int64_t r1 = min((int64_t)a.K, r0 + a.tile_rows);
+    float v = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      if (j + e >= r0 && j + e < r1 && w[e] > 0.f) lp = (int)(j + e);
-    for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-    pick = lp;
+      if (j + e >= r0 && j + e < r1) v += w[e];
+    float x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const float local = target - before;
+    const unsigned hit = force_last ? 0u : __ballot_sync(0xffffffffu, x > local);
+    int pick = -1;
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      if (lane == l) {
+        float acc = x - v;
+        int lastp = -1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (j + e < r0 || j + e >= r1) continue;
+          if (w[e] > 0.f) lastp = (int)(j + e);
+          acc += w[e];
+          if (pick < 0 && acc > local) pick = (int)(j + e);
+        }
+        if (pick < 0) pick = lastp;
+      }
+      pick = __shfl_sync(0xffffffffu, pick, l);
+    } else {
+      // last row with weight in the tile
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j + e >= r0 && j + e < r1 && w[e] > 0.f) lp = (int)(j + e);
+      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+      pick = lp;
+    }
+    if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
   }
-  if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
+
+  // normalise this chunk in place
+  if (a.vec_ok && j + 3 < a.K) {
+    *reinterpret_cast<float4*>(qrow + j) =
+        make_float4(w[0] * invS, w[1] * invS, w[2] * invS, w[3] * invS);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e < a.K) qrow[j + e] = w[e] * invS;
+  }
 }
 
 struct GreedyFinArgs {
@@ -722,9 +729,11 @@ template <int BN>
 int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
                    umma::HeadArgs a, int tiles) {
   constexpr int stage = umma::kABytes + BN * 128;
-  // up to ~110 KB of stages for narrow batches (two CTAs per SM), ~200 KB
+  // up to ~96 KB of stages for narrow batches: two CTAs per SM that still
+  // fit beside the previous draft step's finalize CTAs (so the next
+  // projection can start and prefetch while that finalize runs); ~200 KB
   // for wide ones (one CTA per SM)
-  const int budget = (BN <= 64) ? 110 * 1024 : 200 * 1024;
+  const int budget = (BN <= 64) ? 96 * 1024 : 200 * 1024;
   a.stages = std::max(2, std::min(umma::kMaxStages, budget / stage));
   const size_t smem = (size_t)a.stages * stage + 1024;
   auto k = umma::head_umma_kernel<BN>;
