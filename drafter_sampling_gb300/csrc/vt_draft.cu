@@ -28,11 +28,14 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include "vt_common.cuh"
 #include "vt_internal.h"
 #include "vt_umma.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace vt {
 namespace {
@@ -483,135 +486,256 @@ __global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFin
 // topk_chunk takes 1024 ids and leaves its k best in order; topk_final
 // merges the chunks' lists of a row and converts to log q.
 constexpr int kTopkMax = 32;
-constexpr int kTopkChunk = 1024;
+constexpr int kTkNT = 256;               // 8 warps
+constexpr int kTkE = 16;                 // ids per lane per chunk
+constexpr int kTkSpan = kTkNT * kTkE;    // ids per CTA per pass
+constexpr int kTkMaxCL = 8;              // CTAs per row (one cluster)
+constexpr int kTkInsertMax = 6;          // more passing ids than this: sort them as a batch
 
 struct TopkArgs {
   const float* z2;       // [B][K]
   int B, K, k;
   const float2* part;    // [G][B]
   int G;
-  float2* cand;          // [B][nchunk][k]: (z2, index), -inf / INT_MAX padding
-  int nchunk;
   const int* trim_ids;
   int* out_ids;          // [B][k]
   float* out_logq;       // [B][k]
   int* dev_status;
 };
 
-// warp-wide: the best (value, index) over the lanes' heads; returns the lane
-__device__ __forceinline__ int warp_best_lane(float v, int i) {
-  float bv = v;
-  int bi = i, bl = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float w = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int wi = __shfl_xor_sync(0xffffffffu, bi, o);
-    const int wl = __shfl_xor_sync(0xffffffffu, bl, o);
-    if (umma::argmax_better(bv, bi, w, wi)) {
-      bv = w;
-      bi = wi;
-      bl = wl;
-    }
-  }
-  return bl;
+// (value, index) order of the top-k: higher value first, then lower index
+__device__ __forceinline__ bool vi_before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
 }
 
-__global__ void __launch_bounds__(256) topk_chunk_kernel(TopkArgs a) {
-  __shared__ float sv[8][kTopkMax];
-  __shared__ int si[8][kTopkMax];
-  const int b = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// A warp list: lane l holds the l-th entry of a list of 32 (value, index)
+// pairs.  One compare-exchange stage of a bitonic network between lanes
+// l and l ^ stride; blocks of `size` lanes run best first where
+// (l & size) == 0.
+__device__ __forceinline__ void wl_stage(float& v, int& x, int size, int stride, int lane) {
+  const float pv = __shfl_xor_sync(0xffffffffu, v, stride);
+  const int px = __shfl_xor_sync(0xffffffffu, x, stride);
+  const bool keep_better = ((lane & size) == 0) == ((lane & stride) == 0);
+  if (vi_before(pv, px, v, x) == keep_better) {
+    v = pv;
+    x = px;
+  }
+}
+
+__device__ __forceinline__ void wl_sort(float& v, int& x, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) wl_stage(v, x, size, stride, lane);
+}
+
+// (v, x) <- the 32 best of the sorted lists (v, x) and (yv, yx) given in
+// reverse (lane l holds entry 31 - l), sorted: the lanewise better of the two
+// is a bitonic sequence holding the 32 best of both, which one bitonic merge
+// network sorts
+__device__ __forceinline__ void wl_merge_rev(float& v, int& x, float yv, int yx, int lane) {
+  if (vi_before(yv, yx, v, x)) {
+    v = yv;
+    x = yx;
+  }
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) wl_stage(v, x, 32, stride, lane);
+}
+
+// The drafter's k best per row b in one cluster of C CTAs (blockIdx.x =
+// rank).  Each warp scans chunks of 512 ids (CTA r takes the passes
+// r, r + C, ... of 4096 ids) keeping in a warp list the best entries seen.
+// Per chunk: the k-th best of the 32 lanes' best ids bounds the chunk's k-th
+// best from below, as does the list's k-th entry; the ids not below the
+// better bound (usually about k) are gathered through shared memory, sorted
+// as one warp list and merged into the list.  When more than 32 pass (ties),
+// the chunk goes batch by batch instead: ids that beat the list's k-th entry
+// enter it one at a time, or sorted as a batch when many do.  The warps'
+// lists then merge pairwise through shared memory, the CTAs' lists in CTA 0
+// through distributed shared memory, and lane r of CTA 0's warp 0 writes
+// pick r.  Only the first k entries of a list are exact; they are all that
+// is compared and output.
+__global__ void __launch_bounds__(kTkNT) topk_cluster_kernel(TopkArgs a) {
+  constexpr int NW = kTkNT / 32;
+  __shared__ float sv[NW][32];
+  __shared__ int sx[NW][32];
+  __shared__ MS red[NW];
+  __shared__ float gv[NW][32];  // a warp's gathered candidates
+  __shared__ int gx[NW][32];
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank(), C = (int)cl.num_blocks();
+  const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k1 = a.k - 1;
   griddep_wait();  // the projection has completed
-  // this thread's 4 ids, sorted best first
-  float v[4];
-  int ix[4];
-  const int64_t j0 = (int64_t)c * kTopkChunk + 4 * tid;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int64_t j = j0 + e;
-    v[e] = (j < a.K) ? a.z2[(int64_t)b * a.K + j] : -INFINITY;
-    if (v[e] != v[e]) v[e] = -INFINITY;  // non-finite rows are flagged from the partials
-    ix[e] = (j < a.K) ? (int)j : 0x7fffffff;
-  }
-#pragma unroll
-  for (int p = 0; p < 4; ++p)
-#pragma unroll
-    for (int q = 0; q < 3 - p; ++q)
-      if (umma::argmax_better(v[q], ix[q], v[q + 1], ix[q + 1])) {
-        const float tv = v[q]; v[q] = v[q + 1]; v[q + 1] = tv;
-        const int ti = ix[q]; ix[q] = ix[q + 1]; ix[q + 1] = ti;
-      }
-  // the warp's k best: k rounds over the lanes' heads
-  int head = 0;
-  for (int r = 0; r < a.k; ++r) {
-    const float hv = head < 4 ? v[head] : -INFINITY;
-    const int hi = head < 4 ? ix[head] : 0x7fffffff;
-    const int wl = warp_best_lane(hv, hi);
-    const float bv = __shfl_sync(0xffffffffu, hv, wl);
-    const int bi = __shfl_sync(0xffffffffu, hi, wl);
-    if (lane == 0) {
-      sv[warp][r] = bv;
-      si[warp][r] = bi;
-    }
-    if (lane == wl) ++head;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // merge the 8 warps' lists: lane l < 8 walks list l
-    int h = 0;
-    for (int r = 0; r < a.k; ++r) {
-      const float hv = (lane < 8 && h < a.k) ? sv[lane][h] : -INFINITY;
-      const int hi = (lane < 8 && h < a.k) ? si[lane][h] : 0x7fffffff;
-      const int wl = warp_best_lane(hv, hi);
-      const float bv = __shfl_sync(0xffffffffu, hv, wl);
-      const int bi = __shfl_sync(0xffffffffu, hi, wl);
-      if (lane == 0)
-        a.cand[((int64_t)b * a.nchunk + c) * a.k + r] = make_float2(bv, __int_as_float(bi));
-      if (lane == wl) ++h;
-    }
-  }
-}
+  // the next kernel may start its prologue; it writes only after its own
+  // wait, which waits for this whole grid
+  griddep_launch_dependents();
 
-__global__ void __launch_bounds__(32) topk_final_kernel(TopkArgs a) {
-  const int b = blockIdx.x, lane = threadIdx.x;
-  griddep_wait();
-  // the row's softmax normaliser from the projection's tile partials
+  // CTA 0: this thread's share of the row's softmax normaliser
   MS g{kNegBig, 0.f};
-  for (int t = lane; t < a.G; t += 32) {
-    const float2 p = a.part[(int64_t)t * a.B + b];
-    g = ms_combine(g, MS{p.x, p.y});
-  }
-  g = warp_ms_reduce(g);
-  const bool ok = g.s > 0.f && isfinite(g.s) && isfinite(g.m);
-  // lane l walks the chunk lists l, l + 32, ...; each round takes the best head
-  int head[32];  // a.nchunk <= 1024 (host check)
-  const int per = (a.nchunk + 31) / 32;
-  for (int q = 0; q < per; ++q) head[q] = 0;
-  for (int r = 0; r < a.k; ++r) {
-    float hv = -INFINITY;
-    int hi = 0x7fffffff, hq = -1;
-    for (int q = 0; q < per; ++q) {
-      const int c = lane + 32 * q;
-      if (c >= a.nchunk || head[q] >= a.k) continue;
-      const float2 e = a.cand[((int64_t)b * a.nchunk + c) * a.k + head[q]];
-      if (umma::argmax_better(hv, hi, e.x, __float_as_int(e.y))) {
-        hv = e.x;
-        hi = __float_as_int(e.y);
-        hq = q;
+  if (rank == 0)
+    for (int t = tid; t < a.G; t += kTkNT) {
+      const float2 p = a.part[(int64_t)t * a.B + b];
+      g = ms_combine(g, MS{p.x, p.y});
+    }
+
+  const float* zr = a.z2 + (int64_t)b * a.K;
+  float rv = -INFINITY;  // this warp's list
+  int rx = 0x7fffffff;
+  float tv = -INFINITY;  // its k-th entry
+  int tx = 0x7fffffff;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int64_t base = (int64_t)rank * kTkSpan + 32 * kTkE * warp; base < a.K;
+       base += (int64_t)C * kTkSpan) {
+    float yv[kTkE];
+#pragma unroll
+    for (int e = 0; e < kTkE; ++e) {
+      const int64_t j = base + 32 * e + lane;
+      const float v = (j < a.K) ? zr[j] : -INFINITY;
+      yv[e] = (v == v) ? v : -INFINITY;  // non-finite rows are flagged from the partials
+    }
+    // the lane's best id
+    float bv = -INFINITY;
+    int bx = 0x7fffffff;
+#pragma unroll
+    for (int e = 0; e < kTkE; ++e) {
+      const int64_t j = base + 32 * e + lane;
+      if (j < a.K && vi_before(yv[e], (int)j, bv, bx)) {
+        bv = yv[e];
+        bx = (int)j;
       }
     }
-    const int wl = warp_best_lane(hv, hi);
-    const float bv = __shfl_sync(0xffffffffu, hv, wl);
-    const int bi = __shfl_sync(0xffffffffu, hi, wl);
-    if (lane == wl && hq >= 0) ++head[hq];
-    if (lane == 0) {
-      const bool have = ok && bi >= 0 && bi < a.K;
-      a.out_ids[(int64_t)b * a.k + r] = have ? a.trim_ids[bi] : -1;
-      // log q = (z2 - m) ln 2 - ln S
-      a.out_logq[(int64_t)b * a.k + r] =
-          have ? (bv - g.m) * 0.6931471805599453f - logf(g.s) : __int_as_float(0x7fc00000);
+    if (!__any_sync(0xffffffffu, vi_before(bv, bx, tv, tx))) continue;  // nothing beats the list
+    // cv: the better of the list's k-th entry and the k-th best lane best
+    wl_sort(bv, bx, lane);
+    float cv = __shfl_sync(0xffffffffu, bv, k1);
+    int cx = __shfl_sync(0xffffffffu, bx, k1);
+    if (vi_before(tv, tx, cv, cx)) {
+      cv = tv;
+      cx = tx;
+    }
+    unsigned msk[kTkE];
+    int n = 0;
+#pragma unroll
+    for (int e = 0; e < kTkE; ++e) {
+      const int64_t j = base + 32 * e + lane;
+      msk[e] = __ballot_sync(0xffffffffu, j < a.K && !vi_before(cv, cx, yv[e], (int)j));
+      n += __popc(msk[e]);
+    }
+    if (n <= 32) {
+      int off = 0;
+#pragma unroll
+      for (int e = 0; e < kTkE; ++e) {
+        if ((msk[e] >> lane) & 1u) {
+          const int slot = off + __popc(msk[e] & lt_mask);
+          gv[warp][slot] = yv[e];
+          gx[warp][slot] = (int)(base + 32 * e + lane);
+        }
+        off += __popc(msk[e]);
+      }
+      __syncwarp();
+      float qv = lane < n ? gv[warp][lane] : -INFINITY;
+      int qx = lane < n ? gx[warp][lane] : 0x7fffffff;
+      __syncwarp();
+      wl_sort(qv, qx, lane);
+      if (tx == 0x7fffffff) {  // the list is still empty (its k-th entry is padding)
+        rv = qv;
+        rx = qx;
+      } else {
+        wl_merge_rev(rv, rx, __shfl_sync(0xffffffffu, qv, 31 - lane),
+                     __shfl_sync(0xffffffffu, qx, 31 - lane), lane);
+      }
+      tv = __shfl_sync(0xffffffffu, rv, k1);
+      tx = __shfl_sync(0xffffffffu, rx, k1);
+      continue;
+    }
+#pragma unroll
+    for (int e = 0; e < kTkE; ++e) {
+      const int64_t j = base + 32 * e + lane;
+      const int yx = (j < a.K) ? (int)j : 0x7fffffff;
+      const bool pass = vi_before(yv[e], yx, tv, tx);
+      unsigned m = __ballot_sync(0xffffffffu, pass);
+      if (m == 0u) continue;
+      if (__popc(m) > kTkInsertMax) {
+        float bv = pass ? yv[e] : -INFINITY;
+        int bx = pass ? yx : 0x7fffffff;
+        wl_sort(bv, bx, lane);
+        wl_merge_rev(rv, rx, __shfl_sync(0xffffffffu, bv, 31 - lane),
+                     __shfl_sync(0xffffffffu, bx, 31 - lane), lane);
+      } else {
+        while (m != 0u) {
+          const int src = __ffs(m) - 1;
+          m &= m - 1u;
+          const float cv = __shfl_sync(0xffffffffu, yv[e], src);
+          const int cx = __shfl_sync(0xffffffffu, yx, src);
+          // the entries before the candidate are a prefix of the sorted list
+          const int pos = __popc(__ballot_sync(0xffffffffu, vi_before(rv, rx, cv, cx)));
+          const float uv = __shfl_up_sync(0xffffffffu, rv, 1);
+          const int ux = __shfl_up_sync(0xffffffffu, rx, 1);
+          if (lane == pos) {
+            rv = cv;
+            rx = cx;
+          } else if (lane > pos) {
+            rv = uv;
+            rx = ux;
+          }
+        }
+      }
+      tv = __shfl_sync(0xffffffffu, rv, k1);
+      tx = __shfl_sync(0xffffffffu, rx, k1);
     }
   }
-  if (lane == 0 && !ok) atomicOr(a.dev_status, VT_DEV_NONFINITE);
+  if (rank == 0) g = block_ms_reduce<kTkNT>(g, red);
+
+  // the CTA's warps, pairwise: slot w <- merge(slot w, slot w + h)
+  sv[warp][lane] = rv;
+  sx[warp][lane] = rx;
+  __syncthreads();
+#pragma unroll
+  for (int h = NW / 2; h >= 1; h >>= 1) {
+    if (warp < h) {
+      wl_merge_rev(rv, rx, sv[warp + h][31 - lane], sx[warp + h][31 - lane], lane);
+      sv[warp][lane] = rv;
+      sx[warp][lane] = rx;
+    }
+    __syncthreads();
+  }
+  cl.sync();  // every CTA's list is in its slot 0
+  if (rank == 0 && warp > 0) {
+    // warp c copies CTA c's list (an empty one past the cluster)
+    float v = -INFINITY;
+    int x = 0x7fffffff;
+    if (warp < C) {
+      v = cl.map_shared_rank(&sv[0][0], warp)[lane];
+      x = cl.map_shared_rank(&sx[0][0], warp)[lane];
+    }
+    sv[warp][lane] = v;
+    sx[warp][lane] = x;
+    rv = v;
+    rx = x;
+  }
+  cl.sync();  // CTA 0 has read the other CTAs' lists; they may exit
+  if (rank != 0) return;
+#pragma unroll
+  for (int h = NW / 2; h >= 1; h >>= 1) {
+    if (warp < h) {
+      wl_merge_rev(rv, rx, sv[warp + h][31 - lane], sx[warp + h][31 - lane], lane);
+      sv[warp][lane] = rv;
+      sx[warp][lane] = rx;
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    const bool ok = g.s > 0.f && isfinite(g.s) && isfinite(g.m);
+    if (lane < a.k) {
+      const bool have = ok && rx >= 0 && rx < a.K;
+      a.out_ids[(int64_t)b * a.k + lane] = have ? a.trim_ids[rx] : -1;
+      // log q = (z2 - m) ln 2 - ln S
+      a.out_logq[(int64_t)b * a.k + lane] =
+          have ? (rv - g.m) * 0.6931471805599453f - logf(g.s) : __int_as_float(0x7fc00000);
+    }
+    if (lane == 0 && !ok) atomicOr(a.dev_status, VT_DEV_NONFINITE);
+  }
 }
 
 struct DraftWs {
@@ -925,9 +1049,8 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
 
 extern "C" size_t vt_draft_topk_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t k) {
   if (B < 1 || K < 1 || k < 1 || k > vt::kTopkMax || k > K) return 0;
-  const size_t nchunk = (size_t)(K + vt::kTopkChunk - 1) / vt::kTopkChunk;
   return vt::align_up(vt_draft_workspace_bytes(B, H, K), 256) +
-         vt::align_up((size_t)B * K * 4, 256) + vt::align_up((size_t)B * nchunk * k * 8, 256);
+         vt::align_up((size_t)B * K * 4, 256);
 }
 
 extern "C" int vt_draft_topk(const uint16_t* hidden, int32_t B, int32_t H, const uint16_t* W_trim,
@@ -945,9 +1068,6 @@ extern "C" int vt_draft_topk(const uint16_t* hidden, int32_t B, int32_t H, const
   DraftWs dws = carve_draft(ws, B, K);
   const size_t off_z = align_up(vt_draft_workspace_bytes(B, H, K), 256);
   float* z2 = reinterpret_cast<float*>(ws + off_z);
-  const int nchunk = (K + kTopkChunk - 1) / kTopkChunk;
-  if (nchunk > 32 * 32) return VT_ERR_UNSUPPORTED;  // K > 2^20
-  float2* cand = reinterpret_cast<float2*>(ws + off_z + align_up((size_t)B * K * 4, 256));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int grid = 0, tile_rows = 0;
   st = launch_head(s, hidden, B, H, W_trim, K, VT_LOG2E / temperature, z2, K, dws.part, nullptr,
@@ -960,24 +1080,24 @@ extern "C" int vt_draft_topk(const uint16_t* hidden, int32_t B, int32_t H, const
   a.k = k;
   a.part = dws.part;
   a.G = grid;
-  a.cand = cand;
-  a.nchunk = nchunk;
   a.trim_ids = trim_ids;
   a.out_ids = out_ids;
   a.out_logq = out_logq;
   a.dev_status = dev_status;
+  const int C = (int)std::min<int64_t>(kTkMaxCL, ((int64_t)K + kTkSpan - 1) / kTkSpan);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.stream = s;
-  cfg.gridDim = dim3((unsigned)B, (unsigned)nchunk);
-  cfg.blockDim = dim3(256);
-  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, topk_chunk_kernel, a));
-  cfg.gridDim = dim3((unsigned)B);
-  cfg.blockDim = dim3(32);
-  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, topk_final_kernel, a));
+  cfg.gridDim = dim3((unsigned)C, (unsigned)B);
+  cfg.blockDim = dim3(kTkNT);
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, topk_cluster_kernel, a));
   return VT_OK;
 }

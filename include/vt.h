@@ -214,7 +214,8 @@ int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
  *  out_ids  int32 [B, k]  out: target ids (-1 for a row with non-finite z)
  *  out_logq f32   [B, k]  out: log q of each (NaN for such a row)
  *  dev_status int32 [1]   out: VT_DEV_NONFINITE
- * 1 <= k <= 32, k <= K <= 2^20; T finite and > 0.  Workspace:
+ * 1 <= k <= 32 and k <= K (else VT_ERR_INVALID_ARG); T finite and > 0.
+ * Workspace:
  * vt_draft_topk_workspace_bytes(B, H, K, k) bytes.
  * ---------------------------------------------------------------------- */
 size_t vt_draft_topk_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t k);

@@ -118,7 +118,12 @@ def test_sampling_trees_are_unsupported(vt):
 
 
 # ------------------------------------------------------------------ top-k
-@pytest.mark.parametrize("B,H,K,k", [(5, 64, 1000, 8), (16, 96, 4096, 32), (1, 32, 40, 1)])
+@pytest.mark.parametrize("B,H,K,k", [
+    (5, 64, 1000, 8), (16, 96, 4096, 32), (1, 32, 40, 1),
+    (4, 64, 9000, 5),        # three CTAs per row
+    (3, 64, 70001, 12),      # eight CTAs per row, several passes, a ragged tail
+    (2, 32, 40000, 32),      # the longest lists
+])
 def test_topk_integer_inputs_exact(vt, B, H, K, k):
     g = synthetic.rng(B + K, 71)
     hidden = _bf16_exact(g.integers(-2, 3, (B, H)))
