@@ -35,7 +35,6 @@ constexpr int kABytes = kBM * 128;  // one A stage: 128 rows x 128 bytes
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 26;
-constexpr int kL2Ahead = 20;        // W_trim blocks per tile prefetched into L2 before the wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -77,13 +76,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
-}
-
-// bring a tile of the tensor into L2 only (no shared memory, no barrier)
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
@@ -264,10 +256,6 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
       tma_load_2d(smem + (size_t)kb * stage_bytes, &map_w, ((kb + rot) % nk) * kBK, m0,
                   &full_bar[kb]);
     }
-    // and the next kL2Ahead blocks into L2, so HBM keeps streaming W_trim
-    // while the previous kernel finishes
-    for (int kb = pre; kb < min(nk, pre + kL2Ahead); ++kb)
-      tma_prefetch_l2_2d(&map_w, ((kb + rot) % nk) * kBK, m0);
     griddep_wait();
     for (int kb = 0; kb < pre; ++kb)
       tma_load_2d(smem + (size_t)kb * stage_bytes + kABytes, &map_h, ((kb + rot) % nk) * kBK, 0,
