@@ -151,3 +151,38 @@ def test_block_graph_argument_checks_need_no_gpu(lib):
     assert lib.vt_block_graph_destroy(None) == _lib.VT_OK
     assert lib.vt_block_workspace_bytes(16, 2048, 32768, 128256, 6) >= \
         lib.vt_verify_workspace_bytes(16, 6, 128256, 32768)
+
+
+def test_tree_and_topk_argument_checks_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    fake = ctypes.c_void_p(256)
+    # the drafter's top-k: 1 <= k <= 32 and k <= K, T > 0
+    assert lib.vt_draft_topk_workspace_bytes(16, 2048, 32768, 8) > \
+        lib.vt_draft_workspace_bytes(16, 2048, 32768)
+    for B, K, k in [(16, 32768, 0), (16, 32768, 33), (16, 4, 5), (0, 100, 1)]:
+        assert lib.vt_draft_topk_workspace_bytes(B, 64, K, k) == 0, (B, K, k)
+    for K, k, T in [(100, 0, 1.0), (100, 33, 1.0), (4, 5, 1.0), (100, 8, 0.0),
+                    (100, 8, float("inf"))]:
+        st = lib.vt_draft_topk(fake, 2, 64, fake, fake, K, k, T, fake, fake, fake, fake,
+                               1 << 24, None)
+        assert st == _lib.VT_ERR_INVALID_ARG, (K, k, T)
+    st = lib.vt_draft_topk(fake, 2, 64, fake, None, 100, 8, 1.0, fake, fake, fake, fake,
+                           1 << 24, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # no trim_ids
+    st = lib.vt_draft_topk(fake, 2, 64, fake, fake, 100, 8, 1.0, fake, fake, fake, fake, 16,
+                           None)
+    assert st == _lib.VT_ERR_WORKSPACE            # workspace too small
+    # greedy tree verification: N <= 255 nodes, T == 0 only
+    assert lib.vt_verify_tree_workspace_bytes(16, 32, 128256) > 0
+    st = lib.vt_verify_tree(fake, _lib.VT_F32, 2, 256, 1000, fake, 0, fake, 0.0, fake, fake,
+                            fake, fake, fake, 1 << 24, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # too many nodes
+    st = lib.vt_verify_tree(fake, _lib.VT_F32, 2, 8, 1000, fake, 4, fake, 0.0, fake, fake,
+                            fake, fake, fake, 1 << 24, None)
+    assert st == _lib.VT_ERR_INVALID_ARG          # parent stride shorter than a tree
+    st = lib.vt_verify_tree(fake, _lib.VT_F32, 2, 8, 1000, fake, 0, fake, 0.7, fake, fake,
+                            fake, fake, fake, 1 << 24, None)
+    assert st == _lib.VT_ERR_UNSUPPORTED          # sampling trees
+    st = lib.vt_verify_tree(fake, _lib.VT_F32, 2, 8, 1000, fake, 0, fake, 0.0, fake, fake,
+                            fake, fake, fake, 16, None)
+    assert st == _lib.VT_ERR_WORKSPACE
