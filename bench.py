@@ -52,6 +52,15 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def peak_tensor_tflops():
+    """Dense bf16 tensor peak for a kernel timed alone (the burst figure)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -385,6 +394,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -416,6 +426,7 @@ def main():
     # call (events between calls serialise the launch overlap of consecutive
     # kernels, so this pass is not the timed one)
     peak, peak_kind = peaks()
+    peak_tf = peak_tensor_tflops()
     alg = algorithmic_bytes()
     nev = {"calibrate": 2, "trim": 2, "draft": 2 * GAMMA, "verify": 2}
     nprof = 5
@@ -509,6 +520,13 @@ def main():
                       "verify_c2": run_verify_c2(torch, vt, step, host),
                       **run_tree(torch, vt, step)},
     }
+    if not args.no_configs:
+        line["configs_measured"] = {
+            "note": "the survey's other configurations, each timed as one CUDA graph of calls "
+                    "(no host overhead); not part of the step",
+            "c1_heads": run_c1_heads(torch, vt, step, peak),
+            "c3_calibration": run_c3_calibration(torch, vt, step, peak),
+            "c4_large": run_c4_large(torch, vt, step, peak, peak_tf)}
 
     if not args.no_e2e:
         line["e2e"] = run_e2e(torch, step, host, stream, args, dist, dev, world)
@@ -722,6 +740,189 @@ def run_selection(torch, vt, step, ncalls: int = 20):
                                     "achieved_gbs": algorithmic_bytes()["calibrate"] / (us * 1e-6) / 1e9,
                                     "dev_status": int(step.status[0].item())}
     return out
+
+
+def graph_us(torch, fn, ncalls: int, reps: int = 3):
+    """Median per-call time of `fn` captured ncalls times in one CUDA graph
+    (host overhead excluded), after two warm replays."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(ncalls):
+                fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ts = []
+    for r in range(reps + 2):
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if r >= 2:
+            ts.append(e0.elapsed_time(e1) * 1e3 / ncalls)
+    del g
+    return float(np.median(ts))
+
+
+def run_c1_heads(torch, vt, step, peak, ncalls: int = 24):
+    """The survey's head configuration: one drafting step (projection, softmax,
+    draw) through the trimmed head (K = 32768) and through the full head
+    (K = V = 128256) at B in {1, 8, 16, 64}, H = 2048, T = 1.  Two W_trim
+    copies alternate so that consecutive calls never find theirs in L2 (the
+    full head, 525 MB, exceeds L2 alone)."""
+    dev = step.dev
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    Wt = [step.W_trim, step.W_trim.clone()]
+    full_ids = torch.arange(V, dtype=torch.int32, device=dev)
+    out = {}
+    for Bx in (1, 8, 16, 64):
+        hid = (torch.randn((Bx, H), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+        u = torch.rand(Bx, generator=gen, device=dev)
+        row = {}
+        for name, Ws, ids, Kx in (("trimmed", Wt, step.trim_ids, K), ("full", [step.W], full_ids, V)):
+            q = torch.empty((Bx, Kx), dtype=torch.float32, device=dev)
+            tok = torch.empty(Bx, dtype=torch.int32, device=dev)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            ws = torch.empty(vt.lib().vt_draft_workspace_bytes(Bx, H, Kx), dtype=torch.uint8,
+                             device=dev)
+            it = [0]
+
+            def fn(Ws=Ws, ids=ids, q=q, tok=tok, st=st, ws=ws):
+                it[0] += 1
+                vt.vt_draft_step(hid, Ws[it[0] % len(Ws)], ids, u, 1.0, q=q, tokens=tok,
+                                 dev_status=st, workspace=ws)
+            us = graph_us(torch, fn, ncalls)
+            nbytes = Kx * H * 2 + Bx * H * 2 + Bx * Kx * 4
+            row[name] = {"us_per_step": us, "algorithmic_bytes": nbytes,
+                         "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+                         "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                         "dev_status": int(st.item())}
+            del q, ws
+        row["speedup_full_over_trimmed"] = row["full"]["us_per_step"] / row["trimmed"]["us_per_step"]
+        row["ideal_speedup_bytes"] = (V * H * 2 + Bx * V * 4) / (K * H * 2 + Bx * K * 4)
+        out[f"B{Bx}"] = row
+    del Wt
+    return out
+
+
+def run_c3_calibration(torch, vt, step, peak):
+    """The survey's calibration configuration: the step's 50M Zipf(1.1) ids
+    -> Top-K for K in {8192, 16384, 32768, 65536}, and the row gather of
+    W [128256, 3072] bf16 N(0, 0.02) into W_trim (timed apart: one graph of
+    calls each)."""
+    dev = step.dev
+    H3 = 3072
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12)
+    W3 = (torch.randn((V, H3), generator=gen, device=dev) * 0.02).to(torch.bfloat16) \
+        .view(torch.int16)
+    out = {}
+    for Kc in (8192, 16384, 32768, 65536):
+        counts = torch.empty(V, dtype=torch.int32, device=dev)
+        topk = torch.empty(Kc, dtype=torch.int32, device=dev)
+        st = torch.zeros(2, dtype=torch.int32, device=dev)
+        wsc = torch.empty(vt.lib().vt_calibrate_topk_workspace_bytes(N_CAL, V, Kc),
+                          dtype=torch.uint8, device=dev)
+        Wt = torch.empty((Kc, H3), dtype=torch.int16, device=dev)
+        ti = torch.empty(Kc, dtype=torch.int32, device=dev)
+        im = torch.empty(V, dtype=torch.int32, device=dev)
+        wst = torch.empty(vt.lib().vt_trim_head_workspace_bytes(V, Kc), dtype=torch.uint8,
+                          device=dev)
+
+        def cal():
+            vt.vt_calibrate_topk(step.ids, V, Kc, counts=counts, topk_ids=topk,
+                                 dev_status=st[0:1], workspace=wsc)
+
+        def trim():
+            vt.vt_trim_head(W3, topk, W_trim=Wt, trim_ids=ti, inv_map=im, dev_status=st[1:2],
+                            workspace=wst)
+        us_c = graph_us(torch, cal, 8)
+        us_t = graph_us(torch, trim, 8)
+        bc = N_CAL * 4 + 2 * V * 4 + Kc * 4
+        bt = 2 * Kc * H3 * 2 + Kc * 4 * 2 + V * 4
+        out[f"K{Kc}"] = {"calibrate_us": us_c, "calibrate_gbs": bc / (us_c * 1e-6) / 1e9,
+                         "calibrate_frac": bc / (us_c * 1e-6) / 1e9 / peak,
+                         "trim_us": us_t, "trim_gbs": bt / (us_t * 1e-6) / 1e9,
+                         "trim_frac": bt / (us_t * 1e-6) / 1e9 / peak,
+                         "dev_status": [int(x) for x in st.cpu().tolist()]}
+        del counts, topk, wsc, Wt, ti, im, wst
+    del W3
+    return out
+
+
+def run_c4_large(torch, vt, step, peak, peak_tf):
+    """The survey's large-batch configuration: B=256, gamma=8, V=152064,
+    H=4096, K=38016 trimmed ids, T=0.7.  One drafting step (tcgen05 tiles of
+    256 batch columns) and one verification over bf16 logits; inputs built on
+    the device with the recipe's shape: logits N(0,2) + 3 ln Zipf_1.1(rank),
+    q = softmax over the trimmed ids of (logit + N(0,1)) / T, drafts drawn
+    from q."""
+    dev = step.dev
+    B4, G4, V4, H4, K4, T4 = 256, 8, 152064, 4096, 38016, 0.7
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(13)
+    perm = torch.randperm(V4, generator=gen, device=dev)
+    trim_ids = torch.sort(perm[:K4]).values.to(torch.int32)   # the K4 best ranks, ascending ids
+    inv_map = torch.full((V4,), -1, dtype=torch.int32, device=dev)
+    inv_map[trim_ids.long()] = torch.arange(K4, dtype=torch.int32, device=dev)
+    rank_of = torch.empty(V4, dtype=torch.float64, device=dev)
+    rank_of[perm] = torch.arange(1, V4 + 1, dtype=torch.float64, device=dev)
+    bias = (3.0 * (-1.1 * torch.log(rank_of))).to(torch.float32)
+    logits = (torch.randn((B4, G4 + 1, V4), generator=gen, device=dev) * 2.0 + bias) \
+        .to(torch.bfloat16)
+    x = logits[:, :G4, :].float()[:, :, trim_ids.long()] + \
+        torch.randn((B4, G4, K4), generator=gen, device=dev)
+    q = torch.softmax(x / T4, dim=-1).contiguous()
+    del x
+    draft = trim_ids[torch.multinomial(q.view(-1, K4), 1, generator=gen).view(B4, G4)].contiguous()
+    u_acc = torch.rand((B4, G4), generator=gen, device=dev)
+    u_res = torch.rand((B4, G4 + 1), generator=gen, device=dev)
+    out_tok = torch.empty((B4, G4 + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty(B4, dtype=torch.int32, device=dev)
+    st = torch.zeros(2, dtype=torch.int32, device=dev)
+    wsv = torch.empty(vt.lib().vt_verify_workspace_bytes(B4, G4, V4, K4), dtype=torch.uint8,
+                      device=dev)
+
+    def ver():
+        vt.vt_verify(logits, q, inv_map, draft, u_acc, u_res, T4, out_tokens=out_tok,
+                     out_num_accepted=out_n, dev_status=st[0:1], workspace=wsv)
+    us_v = graph_us(torch, ver, 10)
+    bv = B4 * (G4 + 1) * V4 * 2 + B4 * K4 * 4 + V4 * 4
+    res = {"verify_us": us_v, "verify_algorithmic_bytes": bv,
+           "verify_gbs": bv / (us_v * 1e-6) / 1e9, "verify_frac": bv / (us_v * 1e-6) / 1e9 / peak,
+           "mean_accepted": float(out_n.float().mean().item())}
+    del logits, q, wsv
+    Wt = [(torch.randn((K4, H4), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+          .view(torch.int16) for _ in range(2)]
+    hid = torch.randn((B4, H4), generator=gen, device=dev).to(torch.bfloat16).view(torch.int16)
+    u = torch.rand(B4, generator=gen, device=dev)
+    qd = torch.empty((B4, K4), dtype=torch.float32, device=dev)
+    tok = torch.empty(B4, dtype=torch.int32, device=dev)
+    wsd = torch.empty(vt.lib().vt_draft_workspace_bytes(B4, H4, K4), dtype=torch.uint8,
+                      device=dev)
+    it = [0]
+
+    def drf():
+        it[0] += 1
+        vt.vt_draft_step(hid, Wt[it[0] % 2], trim_ids, u, T4, q=qd, tokens=tok,
+                         dev_status=st[1:2], workspace=wsd)
+    us_d = graph_us(torch, drf, 12)
+    bd = K4 * H4 * 2 + B4 * H4 * 2 + B4 * K4 * 4
+    fl = 2.0 * B4 * K4 * H4
+    res.update({"draft_us": us_d, "draft_algorithmic_bytes": bd,
+                "draft_gbs": bd / (us_d * 1e-6) / 1e9, "draft_frac_hbm": bd / (us_d * 1e-6) / 1e9 / peak,
+                "draft_tflops": fl / (us_d * 1e-6) / 1e12,
+                "draft_frac_tensor": fl / (us_d * 1e-6) / 1e12 / peak_tf,
+                "dev_status": [int(x) for x in st.cpu().tolist()]})
+    del Wt, qd, wsd
+    return res
 
 
 def run_e2e(torch, step, host, stream, args, dist, dev, world):

@@ -849,10 +849,10 @@ bool umma_supported(const uint16_t* hidden, int B, int H, const uint16_t* W) {
          ((reinterpret_cast<uintptr_t>(W) & 15) == 0) && tensor_map_encoder() != nullptr;
 }
 
-template <int BN>
+template <int BN, int TM>
 int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
                    umma::HeadArgs a, int tiles) {
-  constexpr int stage = umma::kABytes + BN * 128;
+  constexpr int stage = TM * umma::kABytes + BN * 128;
   // up to ~96 KB of stages for narrow batches: two CTAs per SM that still
   // fit beside the previous draft step's finalize CTAs (so the next
   // projection can start and prefetch while that finalize runs); ~200 KB
@@ -860,10 +860,10 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
   const int budget = (BN <= 64) ? 96 * 1024 : 200 * 1024;
   a.stages = std::max(2, std::min(umma::kMaxStages, budget / stage));
   const size_t smem = (size_t)a.stages * stage + 1024;
-  auto k = umma::head_umma_kernel<BN>;
+  auto k = umma::head_umma_kernel<BN, TM>;
   VT_RETURN_IF_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.gridDim = dim3((unsigned)((tiles + TM - 1) / TM));
   cfg.blockDim = dim3(umma::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -900,12 +900,14 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   a.greedy = greedy;
   const int tiles = (K + umma::kBM - 1) / umma::kBM;
   *groups_out = tiles;
+  // wide batches: two tiles per CTA share each staged block of hidden states
+  // (at B = 256 the hidden states re-read per 128-row tile outweigh W_trim)
   switch (BN) {
-    case 16: return launch_umma_bn<16>(s, mw, mh, a, tiles);
-    case 32: return launch_umma_bn<32>(s, mw, mh, a, tiles);
-    case 64: return launch_umma_bn<64>(s, mw, mh, a, tiles);
-    case 128: return launch_umma_bn<128>(s, mw, mh, a, tiles);
-    default: return launch_umma_bn<256>(s, mw, mh, a, tiles);
+    case 16: return launch_umma_bn<16, 1>(s, mw, mh, a, tiles);
+    case 32: return launch_umma_bn<32, 1>(s, mw, mh, a, tiles);
+    case 64: return launch_umma_bn<64, 1>(s, mw, mh, a, tiles);
+    case 128: return launch_umma_bn<128, 2>(s, mw, mh, a, tiles);
+    default: return launch_umma_bn<256, 2>(s, mw, mh, a, tiles);
   }
 }
 

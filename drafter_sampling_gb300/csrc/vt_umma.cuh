@@ -195,13 +195,19 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-// one CTA per 128-row tile of W_trim; BN = padded batch (16..256, step 16)
-template <int BN>
+// one CTA per TM consecutive 128-row tiles of W_trim; BN = padded batch
+// (16..256, step 16).  With TM = 2 the two tiles share every staged block of
+// hidden states (two MMAs per step, one TMEM accumulator each), which halves
+// the hidden-state traffic of wide batches.
+template <int BN, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
 head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                  HeadArgs a) {
+  static_assert(TM == 1 || TM == 2, "one or two tiles per CTA");
   constexpr int kBBytes = BN * 128;
-  constexpr uint32_t kCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  constexpr int kAB = TM * kABytes;  // the A (W_trim) part of a stage
+  constexpr int kNeed = TM * BN;     // accumulator columns
+  constexpr uint32_t kCols = kNeed <= 32 ? 32 : (kNeed <= 64 ? 64 : (kNeed <= 128 ? 128 : (kNeed <= 256 ? 256 : 512)));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -214,9 +220,9 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
-  const int stage_bytes = kABytes + kBBytes;
+  const int stage_bytes = kAB + kBBytes;
   const int tile = blockIdx.x;
-  const int m0 = tile * kBM;
+  const int m0 = tile * kBM * TM;
   const int nk = (a.H + kBK - 1) / kBK;
   // tiles start their reduction at different column blocks, so the rows
   // streamed at any moment are spread over column offsets (DRAM channels)
@@ -253,12 +259,14 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
     const int pre = min(S, nk);
     for (int kb = 0; kb < pre; ++kb) {
       mbar_expect_tx(&full_bar[kb], (uint32_t)stage_bytes);
-      tma_load_2d(smem + (size_t)kb * stage_bytes, &map_w, ((kb + rot) % nk) * kBK, m0,
-                  &full_bar[kb]);
+#pragma unroll
+      for (int t = 0; t < TM; ++t)
+        tma_load_2d(smem + (size_t)kb * stage_bytes + t * kABytes, &map_w,
+                    ((kb + rot) % nk) * kBK, m0 + t * kBM, &full_bar[kb]);
     }
     griddep_wait();
     for (int kb = 0; kb < pre; ++kb)
-      tma_load_2d(smem + (size_t)kb * stage_bytes + kABytes, &map_h, ((kb + rot) % nk) * kBK, 0,
+      tma_load_2d(smem + (size_t)kb * stage_bytes + kAB, &map_h, ((kb + rot) % nk) * kBK, 0,
                   &full_bar[kb]);
     int issued = pre;
     bool ok = true;
@@ -271,8 +279,9 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
       uint8_t* sa = smem + (size_t)s * stage_bytes;
       mbar_expect_tx(&full_bar[s], (uint32_t)stage_bytes);
       const int x = ((kb + rot) % nk) * kBK;
-      tma_load_2d(sa, &map_w, x, m0, &full_bar[s]);
-      tma_load_2d(sa + kABytes, &map_h, x, 0, &full_bar[s]);
+#pragma unroll
+      for (int t = 0; t < TM; ++t) tma_load_2d(sa + t * kABytes, &map_w, x, m0 + t * kBM, &full_bar[s]);
+      tma_load_2d(sa + kAB, &map_h, x, 0, &full_bar[s]);
       issued = kb + 1;
     }
     if (!ok) atomicExch(&s_err, 1);
@@ -297,12 +306,16 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
       }
       fence_after_sync();
       const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-      const uint64_t adesc = sw128_desc(sa);
-      const uint64_t bdesc = sw128_desc(sa + kABytes);
+      const uint64_t bdesc = sw128_desc(sa + kAB);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        // +32 bytes along K per 16-element step (descriptor address field is >> 4)
-        mma_bf16(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+      for (int t = 0; t < TM; ++t) {
+        const uint64_t adesc = sw128_desc(sa + t * kABytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // +32 bytes along K per 16-element step (descriptor address field is >> 4)
+          mma_bf16(tmem + (uint32_t)(t * BN), adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       mma_commit(&empty_bar[s]);
     }
@@ -315,56 +328,61 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   griddep_launch_dependents();
   fence_after_sync();
   const int row = warp * 32 + lane;
-  const int j = m0 + row;
-  if (acc_ok) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+  for (int t = 0; t < TM; ++t) {
+    const int j = m0 + t * kBM + row;
+    const int tt = tile * TM + t;  // this 128-row tile
+    if (acc_ok) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * BN + c0), v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int b = c0 + e;
-        const float z = v[e] * a.out_scale;
-        if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
-        if (a.part != nullptr && a.greedy) {
-          float v = (j < a.K) ? (isfinite(z) ? z : __int_as_float(0x7fc00000)) : -INFINITY;
-          int idx = (j < a.K) ? j : 0x7fffffff;
-          warp_argmax(v, idx);
-          if (lane == 0) red[warp][b] = MS{v, __int_as_float(idx)};
-        } else if (a.part != nullptr) {
-          MS m = (j < a.K) ? MS{z, 1.f} : MS{kNegBig, 0.f};
-          m = warp_ms_reduce(m);
-          if (lane == 0) red[warp][b] = m;
-        }
-      }
-    }
-  } else {
-    atomicExch(&s_err, 1);
-  }
-  fence_before_sync();
-  __syncthreads();
-  if (a.part != nullptr && acc_ok) {
-    for (int b = tid; b < a.B && b < BN; b += kThreads) {
-      MS r = red[0][b];
-      if (a.greedy) {
-        float v = r.m;
-        int idx = __float_as_int(r.s);
-        for (int w = 1; w < 4; ++w) {
-          const float wv = red[w][b].m;
-          const int wi = __float_as_int(red[w][b].s);
-          if (argmax_better(v, idx, wv, wi)) {
-            v = wv;
-            idx = wi;
+        for (int e = 0; e < 16; ++e) {
+          const int b = c0 + e;
+          const float z = v[e] * a.out_scale;
+          if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
+          if (a.part != nullptr && a.greedy) {
+            float v = (j < a.K) ? (isfinite(z) ? z : __int_as_float(0x7fc00000)) : -INFINITY;
+            int idx = (j < a.K) ? j : 0x7fffffff;
+            warp_argmax(v, idx);
+            if (lane == 0) red[warp][b] = MS{v, __int_as_float(idx)};
+          } else if (a.part != nullptr) {
+            MS m = (j < a.K) ? MS{z, 1.f} : MS{kNegBig, 0.f};
+            m = warp_ms_reduce(m);
+            if (lane == 0) red[warp][b] = m;
           }
         }
-        a.part[(int64_t)tile * a.B + b] = make_float2(v, __int_as_float(idx));
-      } else {
-        r = ms_combine(r, red[1][b]);
-        r = ms_combine(r, red[2][b]);
-        r = ms_combine(r, red[3][b]);
-        a.part[(int64_t)tile * a.B + b] = make_float2(r.m, r.s);
+      }
+    } else {
+      atomicExch(&s_err, 1);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (a.part != nullptr && acc_ok && m0 + t * kBM < a.K) {
+      for (int b = tid; b < a.B && b < BN; b += kThreads) {
+        MS r = red[0][b];
+        if (a.greedy) {
+          float v = r.m;
+          int idx = __float_as_int(r.s);
+          for (int w = 1; w < 4; ++w) {
+            const float wv = red[w][b].m;
+            const int wi = __float_as_int(red[w][b].s);
+            if (argmax_better(v, idx, wv, wi)) {
+              v = wv;
+              idx = wi;
+            }
+          }
+          a.part[(int64_t)tt * a.B + b] = make_float2(v, __int_as_float(idx));
+        } else {
+          r = ms_combine(r, red[1][b]);
+          r = ms_combine(r, red[2][b]);
+          r = ms_combine(r, red[3][b]);
+          a.part[(int64_t)tt * a.B + b] = make_float2(r.m, r.s);
+        }
       }
     }
+    __syncthreads();  // red is reused by the next tile
   }
   if (tid == 0 && s_err) atomicOr(a.status, VT_DEV_TIMEOUT);
   if (warp == 1) {

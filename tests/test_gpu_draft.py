@@ -99,6 +99,23 @@ def test_draft_step_trimmed_head_full_size(vt, B):
     _check_step(vt, hidden, W, trim_ids, u, 1.0)
 
 
+def test_draft_step_large_batch_full_size(vt):
+    # the large-batch configuration: B=256, H=4096, K=38016 trimmed ids of
+    # V=152064, W_trim N(0,0.02), hidden N(0,1), T = 0.7 (one tcgen05 tile of
+    # 256 batch columns per 128 rows of W_trim)
+    B, H, V, K = 256, 4096, 152064, 38016
+    g = synthetic.rng(90, 0)
+    hidden = synthetic.normal_bf16(g, (B, H), 1.0)
+    W = synthetic.normal_bf16(g, (K, H), 0.02)
+    perm = synthetic.rank_permutation(V)
+    _, trim_ids, _ = synthetic.trimmed_set(V, K, perm)
+    u = synthetic.uniforms(90, 1, B)
+    checked = _check_step(vt, hidden, W, trim_ids, u, 0.7)
+    # with 38016 ids at T = 0.7 most bins are narrower than the 1e-5 boundary
+    # band, so many draws are checked as valid draws rather than compared
+    assert checked >= B // 2
+
+
 def test_full_vocab_head_and_trimmed_consistency(vt):
     # the full-vocabulary head (K = V, identity map) against the oracle, and
     # the trimmed head equal to the full one restricted and renormalised
