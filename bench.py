@@ -61,6 +61,21 @@ def peak_tensor_tflops():
         return 1900.0
 
 
+def max_over_ranks(torch, x: float, dist, dev) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(steps: int, world: int, total_ms: float) -> float:
+    """Verified positions per second over all ranks: each rank verifies
+    B * GAMMA positions per step."""
+    return B * GAMMA * steps * world / (total_ms / 1e3)
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -477,13 +492,9 @@ def main():
     if dist is not None:
         dist.barrier()
     clocks.stop()
-    total_ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, start.elapsed_time(end), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = B * GAMMA * args.steps * world / (total_ms / 1e3)
+    value = whole_job_value(args.steps, world, total_ms)
     status = [int(x) for x in step.status.cpu().tolist()]
     live_us = float(np.mean([g[1].elapsed_time(g[2]) * 1e3 for g in groups if g is not None])) \
         / CALLS_PER_STEP[dominant]
@@ -958,13 +969,9 @@ def run_e2e(torch, step, host, stream, args, dist, dev, world):
         one(k)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, e0.elapsed_time(e1), dist, dev)
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    return {"value": B * GAMMA * nsteps * world / (ms / 1e3), "unit": UNIT,
+    return {"value": whole_job_value(nsteps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * 4,
             "steps": nsteps}
 
