@@ -684,6 +684,9 @@ __global__ void __launch_bounds__(kNT) verify_greedy_finish_kernel(VArgs a) {
 // deepest accepted node (ties to the lower node) and the choice there.
 constexpr int kMaxTreeNodes = 255;
 
+// one warp per row of partials (up to 32 rows at once)
+constexpr int kTreeNT = 1024;
+
 struct TreeArgs {
   const int* parent;    // [B][N], or one shared [N] when pstride == 0
   int64_t pstride;
@@ -692,16 +695,24 @@ struct TreeArgs {
   int* out_path;        // [B][N] or nullptr
 };
 
-__global__ void __launch_bounds__(kNT) verify_tree_finish_kernel(VArgs a, TreeArgs t) {
+__global__ void __launch_bounds__(kTreeNT) verify_tree_finish_kernel(VArgs a, TreeArgs t) {
   __shared__ int choice[kMaxTreeNodes + 1];
   __shared__ unsigned char acc[kMaxTreeNodes];
   __shared__ unsigned char dep[kMaxTreeNodes];
   __shared__ int path[kMaxTreeNodes];
+  __shared__ int spar[kMaxTreeNodes];  // the tree, staged once: the walk below
+  __shared__ int stok[kMaxTreeNodes];  // is serial, so it reads shared memory only
   __shared__ int s_best, s_len, s_flags;
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.R, N = t.N;
+  // inputs that the stats kernel of this call does not write (every older
+  // kernel has completed): fetch before waiting
+  for (int i = tid; i < N; i += kTreeNT) {
+    spar[i] = t.parent[(int64_t)b * t.pstride + i];
+    stok[i] = t.tokens[(int64_t)b * N + i];
+  }
   griddep_wait();  // the stats kernel has completed
-  for (int i = warp; i < R; i += kNT / 32) {
+  for (int i = warp; i < R; i += kTreeNT / 32) {
     float v = -INFINITY;
     int idx = 0x7fffffff;
     const float2* pp = a.part + ((int64_t)b * R + i) * a.C1;
@@ -721,11 +732,9 @@ __global__ void __launch_bounds__(kNT) verify_tree_finish_kernel(VArgs a, TreeAr
     int flags = 0, best = -1, best_depth = 0;
     for (int r = 0; r < R; ++r)
       if (choice[r] < 0) flags |= VT_DEV_NONFINITE;
-    const int* par = t.parent + (int64_t)b * t.pstride;
-    const int* tok = t.tokens + (int64_t)b * N;
     for (int i = 0; i < N && !flags; ++i) {
-      const int p = par[i];
-      const int x = tok[i];
+      const int p = spar[i];
+      const int x = stok[i];
       if (p < -1 || p >= i || x < 0 || (int64_t)x >= a.V) {
         flags |= VT_DEV_BAD_DRAFT;
         break;
@@ -740,7 +749,7 @@ __global__ void __launch_bounds__(kNT) verify_tree_finish_kernel(VArgs a, TreeAr
     }
     int len = 0;
     if (!flags) {
-      for (int i = best; i >= 0; i = par[i]) path[len++] = i;
+      for (int i = best; i >= 0; i = spar[i]) path[len++] = i;
       for (int k = 0; k < len / 2; ++k) {  // root first
         const int tmp = path[k];
         path[k] = path[len - 1 - k];
@@ -753,16 +762,16 @@ __global__ void __launch_bounds__(kNT) verify_tree_finish_kernel(VArgs a, TreeAr
   }
   __syncthreads();
   const int flags = s_flags, len = s_len, best = s_best;
-  for (int i = tid; i < R; i += kNT) {
+  for (int i = tid; i < R; i += kTreeNT) {
     int v = -1;
     if (!flags) {
-      if (i < len) v = t.tokens[(int64_t)b * N + path[i]];
+      if (i < len) v = stok[path[i]];
       else if (i == len) v = choice[best + 1];
     }
     a.out_tokens[(int64_t)b * R + i] = v;
   }
   if (t.out_path != nullptr)
-    for (int i = tid; i < N; i += kNT)
+    for (int i = tid; i < N; i += kTreeNT)
       t.out_path[(int64_t)b * N + i] = (!flags && i < len) ? path[i] : -1;
   if (tid == 0) {
     a.out_n[b] = flags ? 0 : len;
@@ -784,7 +793,7 @@ int launch_verify_tree(const VArgs& a, const TreeArgs& t, cudaStream_t s) {
                                dim3((unsigned)((int64_t)a.B * a.R), (unsigned)a.C1), s, a));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.B);
-  cfg.blockDim = dim3(kNT);
+  cfg.blockDim = dim3(kTreeNT);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
