@@ -533,8 +533,8 @@ def main():
     }
     if not args.no_configs:
         line["configs_measured"] = {
-            "note": "the survey's other configurations, each timed as one CUDA graph of calls "
-                    "(no host overhead); not part of the step",
+            "note": "the head, calibration and large-batch configurations, each timed as one "
+                    "CUDA graph of calls (no host overhead); not part of the step",
             "c1_heads": run_c1_heads(torch, vt, step, peak),
             "c3_calibration": run_c3_calibration(torch, vt, step, peak),
             "c4_large": run_c4_large(torch, vt, step, peak, peak_tf)}
@@ -782,7 +782,7 @@ def graph_us(torch, fn, ncalls: int, reps: int = 3):
 
 
 def run_c1_heads(torch, vt, step, peak, ncalls: int = 24):
-    """The survey's head configuration: one drafting step (projection, softmax,
+    """The head configuration: one drafting step (projection, softmax,
     draw) through the trimmed head (K = 32768) and through the full head
     (K = V = 128256) at B in {1, 8, 16, 64}, H = 2048, T = 1.  Two W_trim
     copies alternate so that consecutive calls never find theirs in L2 (the
@@ -824,7 +824,7 @@ def run_c1_heads(torch, vt, step, peak, ncalls: int = 24):
 
 
 def run_c3_calibration(torch, vt, step, peak):
-    """The survey's calibration configuration: the step's 50M Zipf(1.1) ids
+    """The calibration configuration: the step's 50M Zipf(1.1) ids
     -> Top-K for K in {8192, 16384, 32768, 65536}, and the row gather of
     W [128256, 3072] bf16 N(0, 0.02) into W_trim (timed apart: one graph of
     calls each)."""
@@ -869,7 +869,7 @@ def run_c3_calibration(torch, vt, step, peak):
 
 
 def run_c4_large(torch, vt, step, peak, peak_tf):
-    """The survey's large-batch configuration: B=256, gamma=8, V=152064,
+    """The large-batch configuration: B=256, gamma=8, V=152064,
     H=4096, K=38016 trimmed ids, T=0.7.  One drafting step (tcgen05 tiles of
     256 batch columns) and one verification over bf16 logits; inputs built on
     the device with the recipe's shape: logits N(0,2) + 3 ln Zipf_1.1(rank),
