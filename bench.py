@@ -153,9 +153,9 @@ class HostInputs:
         self.u_resample = vi["u_resample"]
         # the workload's own drafter distributions and drafts (correlated
         # with the logits), for the verify-only line and tau
-        self.q_c2 = vi["q"]
-        self.draft_c2 = vi["draft"]
-        self.inv_map_c2 = vi["inv_map"]
+        self.q_verify = vi["q"]
+        self.draft_verify = vi["draft"]
+        self.inv_map_verify = vi["inv_map"]
 
     def step_inputs(self):
         return dict(ids=self.ids, W=self.W, hidden=self.hidden, u_draft=self.u_draft,
@@ -528,16 +528,16 @@ def main():
         "next_rows": {"greedy_block": run_greedy_block(torch, vt, step),
                       **run_selection(torch, vt, step),
                       "block_graph": run_block_graph(torch, vt, step),
-                      "verify_c2": run_verify_c2(torch, vt, step, host),
+                      "verify_batched": run_verify_batched(torch, vt, step, host),
                       **run_tree(torch, vt, step)},
     }
     if not args.no_configs:
         line["configs_measured"] = {
             "note": "the head, calibration and large-batch configurations, each timed as one "
                     "CUDA graph of calls (no host overhead); not part of the step",
-            "c1_heads": run_c1_heads(torch, vt, step, peak),
-            "c3_calibration": run_c3_calibration(torch, vt, step, peak),
-            "c4_large": run_c4_large(torch, vt, step, peak, peak_tf)}
+            "trimmed_vs_full_head": run_head_batches(torch, vt, step, peak),
+            "calibration_H3072": run_calibration_h3072(torch, vt, step, peak),
+            "large_batch_B256": run_large_batch(torch, vt, step, peak, peak_tf)}
 
     if not args.no_e2e:
         line["e2e"] = run_e2e(torch, step, host, stream, args, dist, dev, world)
@@ -643,13 +643,13 @@ def run_tree(torch, vt, step, ncalls: int = 100):
     return res
 
 
-def run_verify_c2(torch, vt, step, host, ncalls: int = 200):
+def run_verify_batched(torch, vt, step, host, ncalls: int = 200):
     """vt_verify alone on the batched-verify workload's own q and drafts
     (q = softmax over the trimmed ids of logit + N(0,1), drafts drawn from
     q): verified positions/s of the verify call and tau = mean tokens per
     block (accepted + 1)."""
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(step.dev)
-    q, draft, inv_map = t(host.q_c2), t(host.draft_c2), t(host.inv_map_c2)
+    q, draft, inv_map = t(host.q_verify), t(host.draft_verify), t(host.inv_map_verify)
 
     def call(k):
         s = step.vsets[k % step.nsets]
@@ -781,7 +781,7 @@ def graph_us(torch, fn, ncalls: int, reps: int = 3):
     return float(np.median(ts))
 
 
-def run_c1_heads(torch, vt, step, peak, ncalls: int = 24):
+def run_head_batches(torch, vt, step, peak, ncalls: int = 24):
     """The head configuration: one drafting step (projection, softmax,
     draw) through the trimmed head (K = 32768) and through the full head
     (K = V = 128256) at B in {1, 8, 16, 64}, H = 2048, T = 1.  Two W_trim
@@ -823,7 +823,7 @@ def run_c1_heads(torch, vt, step, peak, ncalls: int = 24):
     return out
 
 
-def run_c3_calibration(torch, vt, step, peak):
+def run_calibration_h3072(torch, vt, step, peak):
     """The calibration configuration: the step's 50M Zipf(1.1) ids
     -> Top-K for K in {8192, 16384, 32768, 65536}, and the row gather of
     W [128256, 3072] bf16 N(0, 0.02) into W_trim (timed apart: one graph of
@@ -868,7 +868,7 @@ def run_c3_calibration(torch, vt, step, peak):
     return out
 
 
-def run_c4_large(torch, vt, step, peak, peak_tf):
+def run_large_batch(torch, vt, step, peak, peak_tf):
     """The large-batch configuration: B=256, gamma=8, V=152064,
     H=4096, K=38016 trimmed ids, T=0.7.  One drafting step (tcgen05 tiles of
     256 batch columns) and one verification over bf16 logits; inputs built on
