@@ -76,6 +76,10 @@ hist_sample_kernel(const int* __restrict__ ids, int64_t ns, int V, unsigned* __r
     }
   }
   __syncthreads();
+  // the ids are read above without waiting (no kernel just before this one
+  // writes them); the sample table they are added to is zeroed by it
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = threadIdx.x; i < kHashSlots; i += kSampleNT) {
     const int id = hkey[i];
     if (id >= 0) atomicAdd(tmp + id, hval[i]);
@@ -93,6 +97,8 @@ hot_select_kernel(const unsigned* __restrict__ tmp, int V, unsigned thr, int* __
   __shared__ int wcnt[kSelNT / 32];
   __shared__ unsigned long long wkey[kSelNT / 32];
   __shared__ int sbase;
+  griddep_wait();  // the sample counts are complete
+  griddep_launch_dependents();
   const int i = blockIdx.x * kSelNT + threadIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned c = (i < V) ? tmp[i] : 0u;
@@ -154,6 +160,10 @@ hist_main_kernel(const int* __restrict__ ids, int64_t n, int V, const int* __res
   if (HOT) {
     for (int w = tid; w <= nwords; w += kMainNT) lut[w] = 0u;
     for (int h = tid; h < kHotMax; h += kMainNT) hcnt[h] = 0u;
+  }
+  griddep_wait();  // the hot ids are selected and the counts zeroed
+  griddep_launch_dependents();
+  if (HOT) {
     const unsigned long long tk = *top_key;
     if (tk != 0ull) {
       top = 0xffffffffu - (unsigned)(tk & 0xffffffffull);
@@ -528,6 +538,8 @@ __global__ void calib_zero_kernel(unsigned* __restrict__ counts, unsigned* __res
                                   int* __restrict__ hot_n, unsigned long long* __restrict__ top_key,
                                   int* __restrict__ dev_status, unsigned* __restrict__ zero_words,
                                   int64_t nzero) {
+  griddep_wait();  // the previous kernel may still read what is zeroed here
+  griddep_launch_dependents();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t i = t0; i < V; i += stride) {
@@ -931,21 +943,21 @@ int calibrate_impl(const int32_t* ids, int64_t n, int32_t V, int32_t K, uint32_t
   const int64_t nzero = calib_zero_words(V, plan);
   const int64_t zwork = std::max<int64_t>(V, nzero);
   const int zgrid = (int)std::min<int64_t>((zwork + 255) / 256, 4096);
-  calib_zero_kernel<<<zgrid, 256, 0, s>>>(counts, ws.tmp, V, ws.hot_n, ws.top_key, dev_status,
-                                          ws.zero_base, nzero);
-  VT_RETURN_IF_LAUNCH_FAILED();
+  VT_RETURN_IF_CUDA(launch_pdl(calib_zero_kernel, dim3((unsigned)zgrid), dim3(256), 0, s, counts,
+                               ws.tmp, (int)V, ws.hot_n, ws.top_key, dev_status, ws.zero_base,
+                               nzero));
   if (n > 0) {
     const int vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
     const int use_hot = V <= kHotBitmapMaxV;
     if (use_hot) {
       const int64_t ns = std::min<int64_t>(n, kSample);
       const unsigned thr = kSampleThr;
-      hist_sample_kernel<<<(unsigned)((ns + kSampleIds - 1) / kSampleIds), kSampleNT, 0, s>>>(
-          ids, ns, V, ws.tmp);
-      VT_RETURN_IF_LAUNCH_FAILED();
-      hot_select_kernel<<<(V + kSelNT - 1) / kSelNT, kSelNT, 0, s>>>(ws.tmp, V, thr, ws.hot_list,
-                                                                      ws.hot_n, ws.top_key);
-      VT_RETURN_IF_LAUNCH_FAILED();
+      VT_RETURN_IF_CUDA(launch_pdl(hist_sample_kernel,
+                                   dim3((unsigned)((ns + kSampleIds - 1) / kSampleIds)),
+                                   dim3(kSampleNT), 0, s, ids, ns, (int)V, ws.tmp));
+      VT_RETURN_IF_CUDA(launch_pdl(hot_select_kernel, dim3((unsigned)((V + kSelNT - 1) / kSelNT)),
+                                   dim3(kSelNT), 0, s, (const unsigned*)ws.tmp, (int)V, thr,
+                                   ws.hot_list, ws.hot_n, ws.top_key));
     }
     const int64_t want = (n / 4 + kMainNT - 1) / kMainNT;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms()));
@@ -954,13 +966,16 @@ int calibrate_impl(const int32_t* ids, int64_t n, int32_t V, int32_t K, uint32_t
       VT_RETURN_IF_CUDA(cudaFuncSetAttribute(hist_main_kernel<true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem));
-      hist_main_kernel<true><<<grid, kMainNT, smem, s>>>(ids, n, V, ws.hot_list, ws.hot_n,
-                                                         ws.top_key, counts, dev_status, vec_ok);
+      VT_RETURN_IF_CUDA(launch_pdl(hist_main_kernel<true>, dim3((unsigned)grid), dim3(kMainNT),
+                                   smem, s, ids, n, (int)V, (const int*)ws.hot_list,
+                                   (const int*)ws.hot_n, (const unsigned long long*)ws.top_key,
+                                   counts, dev_status, vec_ok));
     } else {
-      hist_main_kernel<false><<<grid, kMainNT, 0, s>>>(ids, n, V, ws.hot_list, ws.hot_n,
-                                                       ws.top_key, counts, dev_status, vec_ok);
+      VT_RETURN_IF_CUDA(launch_pdl(hist_main_kernel<false>, dim3((unsigned)grid), dim3(kMainNT),
+                                   0, s, ids, n, (int)V, (const int*)ws.hot_list,
+                                   (const int*)ws.hot_n, (const unsigned long long*)ws.top_key,
+                                   counts, dev_status, vec_ok));
     }
-    VT_RETURN_IF_LAUNCH_FAILED();
   }
 
   // Top-K: radix sort of (~count, id), one launch per pass
