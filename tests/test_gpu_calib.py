@@ -39,6 +39,7 @@ def _calib(vt, ids, V, K):
     (17, 9, 5, 1.1),                # many zero counts (ties at 0)
     (300_000, 2_100_000, 20_000, 1.1),  # counts need 22 bits: three sort passes, 37 tiles
     (600_000, 1_000_003, 4096, 1.0),    # V beyond the shared-memory hot-id table
+    (1 << 22, 2_000_000, 4096, 1.05),   # the largest vocabulary the sort takes
 ])
 def test_histogram_and_topk_bit_exact(vt, V, N, K, s):
     ids = synthetic.zipf_ids(N, V, s=s, seed=V + N)
@@ -125,7 +126,8 @@ def test_calibration_full_size(vt):
 
 @pytest.mark.parametrize("V,H,K", [(500, 24, 77), (1000, 13, 999), (64, 8, 64), (300, 3072, 1),
                                    (70_001, 16, 40_000),       # K above one index-kernel batch
-                                   ((1 << 20) + 37, 8, 5000)])  # V above the one-CTA index mapper
+                                   ((1 << 20) + 37, 8, 5000),   # V above the one-CTA index mapper
+                                   (1 << 22, 8, 3000)])         # the largest vocabulary
 def test_trim_head_bit_exact(vt, V, H, K):
     g = synthetic.rng(V + H + K, 0)
     W = g.integers(0, 65535, (V, H)).astype(np.uint16)

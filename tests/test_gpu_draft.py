@@ -69,6 +69,7 @@ SHAPES = [
     (17, 256, 3000, 1.3),    # two batch tiles
     (64, 512, 2000, 1.0),    # four batch tiles
     (2, 8, 1, 1.0),          # K = 1
+    (2, 65536, 64, 1.0),     # the largest hidden size
 ]
 
 

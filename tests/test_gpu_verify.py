@@ -97,6 +97,7 @@ CASES = [
     (3, 64, 2048, 256, "bf16", 1.0, 0.3),    # the largest gamma
     (2, 2, 262144, 5000, "f32", 1.0, 1.0),   # a large vocabulary: 128 residual tiles
     (2, 3, 200003, 3000, "bf16", 0.9, 1.0),  # a large ragged vocabulary
+    (1, 1, 1 << 22, 4096, "f32", 1.0, 1.0),  # the largest vocabulary: 2048 residual tiles
 ]
 
 
