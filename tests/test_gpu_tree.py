@@ -213,3 +213,25 @@ def test_an_eagle_style_tree_end_to_end(vt):
     ref = verify_tree_greedy(logits, par, tok)
     assert np.array_equal(out, ref.tokens) and np.array_equal(n, ref.num_accepted)
     assert (n >= 1).all()
+
+
+def test_topk_non_finite_row_is_flagged(vt):
+    # a NaN hidden state makes row 1's logits non-finite: its picks are -1
+    # with NaN log q and the status flags it; the other rows are unaffected
+    g = synthetic.rng(9, 74)
+    B, H, K, k = 3, 64, 3000, 8
+    hidden = synthetic.normal_bf16(g, (B, H), 1.0).copy()
+    hidden[1, 5] = 0x7FC0                      # bf16 NaN
+    W = synthetic.normal_bf16(g, (K, H), 0.1)
+    trim_ids = np.sort(g.permutation(2 * K)[:K]).astype(np.int32)
+    ids, logq, st = vt.vt_draft_topk(_dev(hidden.view(np.int16)), _dev(W.view(np.int16)),
+                                     _dev(trim_ids), k, 1.0)
+    torch.cuda.synchronize()
+    assert int(st.item()) & vt.VT_DEV_NONFINITE
+    ids, logq = ids.cpu().numpy(), logq.cpu().numpy()
+    assert (ids[1] == -1).all() and np.isnan(logq[1]).all()
+    keep = [0, 2]
+    ref = draft_topk(hidden[keep], W, trim_ids, k, 1.0)
+    assert np.array_equal(ids[keep], ref["ids"])
+    err = np.abs(logq[keep] - ref["logq"])
+    assert (err <= 1e-3 * np.maximum(1.0, np.abs(ref["logq"]))).all()
