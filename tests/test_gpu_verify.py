@@ -250,3 +250,26 @@ def test_toy_chain_exact_and_chi_square(vt):
         stat += float(((counts[c] - e) ** 2 / e).sum())
         dof += V - 1
     assert stats.chi2.sf(stat, dof) > 1e-3
+
+
+def test_parity_largest_batch(vt):
+    # B = 65535 sequences (the largest grid the entry point takes), gamma = 1,
+    # V = 64: a seeded base set of 1024 sequences repeated; every sequence is
+    # compared with the oracle's result for its base sequence
+    import dataclasses
+    base = synthetic.verify_inputs(B=1024, gamma=1, V=64, K=16, seed=7)
+    B = 65535
+    reps = -(-B // 1024)
+    d = dict(base)
+    for k in ("logits", "q", "draft", "u_accept", "u_resample"):
+        d[k] = np.ascontiguousarray(np.concatenate([base[k]] * reps)[:B])
+    toks, n, acc, st = _run(vt, d)
+    assert st == 0
+    ref = _oracle(base)
+    tiled = {}
+    for f in dataclasses.fields(ref):
+        v = getattr(ref, f.name)
+        tiled[f.name] = np.concatenate([v] * reps)[:B] if isinstance(v, np.ndarray) else v
+    ref_big = dataclasses.replace(ref, **tiled)
+    s = compare_verify(toks, n, acc, ref_big, draw_weights=_weights(d))
+    assert s["compared"] >= B - 64 * reps, s
