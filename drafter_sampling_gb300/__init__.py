@@ -17,7 +17,7 @@ from ._lib import (VT_BF16, VT_DEV_BAD_DRAFT, VT_DEV_BAD_ID,  # noqa: F401
                    VT_DEV_ZERO_RESIDUAL, VT_F32,
                    VtError)
 
-__all__ = ["vt_calibrate_topk", "vt_calibrate_top_p", "vt_calibrate_min_count", "vt_trim_head",
+__all__ = ["vt_selftest_wait", "vt_calibrate_topk", "vt_calibrate_top_p", "vt_calibrate_min_count", "vt_trim_head",
            "vt_draft_logits", "vt_draft_step", "vt_draft_topk", "vt_verify", "vt_verify_tree",
            "BlockGraph",
            "workspace_bytes",
@@ -401,6 +401,26 @@ def vt_verify_tree(target_logits, parent, tokens, temperature: float = 0.0, out_
                           _stream_ptr(stream))
     _lib.check("vt_verify_tree", st)
     return out_tokens, out_num_accepted, out_path, dev_status
+
+
+def vt_selftest_wait(which: int, limit: int, flag=None, dev_status=None, stream=None):
+    """Runs one of the library's bounded device waits on an object that
+    nothing completes (which 0: an mbarrier; 1: the same after one arrival,
+    the control; 2: a published flag, int32 [1] on the device) for at most
+    `limit` polls.  VT_DEV_TIMEOUT is OR-ed into dev_status (int32 [1],
+    zeroed here when not given) when the wait gives up."""
+    torch = _torch()
+    if dev_status is None:
+        dev = flag.device if flag is not None else torch.device("cuda", torch.cuda.current_device())
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _dev(dev_status, "dev_status", (torch.int32,), 1)
+    if flag is not None:
+        _dev(flag, "flag", (torch.int32, torch.uint32), 1)
+    st = lib().vt_selftest_wait(int(which), int(limit),
+                                flag.data_ptr() if flag is not None else None,
+                                dev_status.data_ptr(), _stream_ptr(stream))
+    _lib.check("vt_selftest_wait", st)
+    return dev_status
 
 
 class BlockGraph:

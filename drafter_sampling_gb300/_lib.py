@@ -53,6 +53,7 @@ class BlockDesc(C.Structure):
 SIGNATURES = {
     "vt_status_string": (C.c_char_p, [C.c_int]),
     "vt_abi_version": (C.c_int, []),
+    "vt_selftest_wait": (C.c_int, [_i32, C.c_uint32, _p, _p, _p]),
     "vt_calibrate_topk_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "vt_calibrate_topk": (C.c_int, [_p, _i64, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "vt_calibrate_select_workspace_bytes": (_sz, [_i64, _i32]),

@@ -292,6 +292,9 @@ constexpr int kRsWarps = kRsNT / 32;
 constexpr int kRsMaxD = 10;                  // digit bits: radix <= 1024
 constexpr int kRsMaxPasses = 4;
 constexpr int kRsMaxV = 1 << 22;
+// reads of an unpublished digit count before a tile gives up (a relaxed L2
+// read takes ~160 ns when nothing else runs: under a second in all, since
+// a thread that gave up once polls no further count)
 constexpr uint32_t kRsSpinLimit = 1u << 22;
 
 struct SortPlan {
@@ -353,11 +356,6 @@ sort_hist_kernel(const unsigned* __restrict__ counts, int V, int passes, int D,
     if (sh[i]) atomicAdd(ghist + i, sh[i]);
 }
 
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -493,7 +491,7 @@ __global__ void __launch_bounds__(kRsNT, 1) sort_pass_kernel(SortPassArgs a) {
       for (int j = 0; j < 16; ++j) {
         const int t = t0 + j * tpd;
         const unsigned* sp = a.status + (int64_t)t * R + d;
-        for (uint32_t it = 0; (v[j] >> 31) == 0u && it < kRsSpinLimit; ++it) v[j] = ld_relaxed_u32(sp);
+        v[j] = poll_published(sp, v[j], timed_out ? 0u : kRsSpinLimit);
         if ((v[j] >> 31) == 0u) timed_out = true;
         part += v[j] & 0x7fffffffu;
       }

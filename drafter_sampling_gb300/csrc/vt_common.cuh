@@ -28,6 +28,20 @@ namespace vt {
 // segment holds only -inf logits.
 constexpr float kNegBig = -3.402823466e38f;
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A word that another thread block publishes by setting bit 31: re-read `p`
+// (whose last value read is v) until bit 31 is set or `limit` reads have
+// passed; returns the last value (bit 31 clear: the wait gave up).
+__device__ __forceinline__ unsigned poll_published(const unsigned* p, unsigned v, uint32_t limit) {
+  for (uint32_t it = 0; (v >> 31) == 0u && it < limit; ++it) v = ld_relaxed_u32(p);
+  return v;
+}
+
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

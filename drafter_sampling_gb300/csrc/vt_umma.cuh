@@ -34,7 +34,11 @@ constexpr int kBK = 64;             // reduction elements per stage (128 bytes)
 constexpr int kABytes = kBM * 128;  // one A stage: 128 rows x 128 bytes
 constexpr int kMaxStages = 8;
 constexpr int kThreads = 128;
-constexpr uint32_t kWaitLimit = 1u << 26;
+// polls of an mbarrier before a wait gives up: an incomplete try_wait
+// suspends for ~3.8 us on sm_103a, so this is about one second, far above
+// any wait of a working pipeline (the longest, the epilogue's wait for the
+// whole reduction, lasts tens of microseconds)
+constexpr uint32_t kWaitLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -62,9 +66,15 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// bounded wait for the phase with the given parity to complete
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// bounded wait for the phase with the given parity to complete: false once
+// `limit` polls have found it incomplete
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try(bar, parity)) return true;
   return false;
 }

@@ -68,8 +68,10 @@ enum {
   VT_DEV_NONFINITE = 8,      /* NaN/Inf reached a softmax normaliser           */
   VT_DEV_ZERO_RESIDUAL = 16, /* informational: residual mass was zero at a
                                 rejection; that draw used p instead            */
-  VT_DEV_TIMEOUT = 32        /* an internal wait between thread blocks gave up
-                                (bounded spin); the affected outputs are unset */
+  VT_DEV_TIMEOUT = 32        /* a bounded internal wait gave up after about a
+                                second (a pipeline mbarrier, or a count another
+                                thread block publishes); the affected outputs
+                                are unset                                       */
 };
 
 /* Human-readable text for a return code. Never NULL. */
@@ -408,6 +410,29 @@ size_t vt_block_workspace_bytes(int32_t B, int32_t H, int32_t K, int32_t V, int3
 int vt_block_graph_create(const vt_block_desc* desc, void** graph);
 int vt_block_graph_launch(void* graph, void* stream);
 int vt_block_graph_destroy(void* graph);
+
+/* ---------------------------------------------------------------------------
+ * vt_selftest_wait — failure detection self-test of the bounded waits.
+ *
+ * Not part of the method: it runs, in one thread of one thread block, the
+ * same device wait helpers the kernels above use between thread blocks,
+ * with a caller-chosen iteration limit, so a test can make a wait give up
+ * without anything hanging, and check that the status word says so.
+ *   which 0: wait on an mbarrier that nothing arrives on (the wait helper
+ *            of the tcgen05 pipelines) -- always gives up;
+ *   which 1: the same mbarrier after one arrival -- completes;
+ *   which 2: poll *flag until bit 31 is set (the helper with which a radix
+ *            sort tile waits for the digit counts of earlier tiles) -- gives
+ *            up unless bit 31 of *flag is set.
+ * limit    polls before giving up, 1 <= limit <= 2^20.
+ * flag     uint32 [1] device, read only (which 2; may be NULL otherwise).
+ * dev_status int32 [1] device: VT_DEV_TIMEOUT is OR-ed in when the wait
+ *          gives up; nothing else is written.
+ * Returns VT_ERR_INVALID_ARG for another `which`, a limit out of range, or a
+ * missing pointer; VT_ERR_CUDA if the launch fails.  Asynchronous on `stream`.
+ */
+int vt_selftest_wait(int32_t which, uint32_t limit, const uint32_t* flag, int32_t* dev_status,
+                     void* stream);
 
 #ifdef __cplusplus
 }

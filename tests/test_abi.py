@@ -186,3 +186,15 @@ def test_tree_and_topk_argument_checks_need_no_gpu(lib):
     st = lib.vt_verify_tree(fake, _lib.VT_F32, 2, 8, 1000, fake, 0, fake, 0.0, fake, fake,
                             fake, fake, fake, 16, None)
     assert st == _lib.VT_ERR_WORKSPACE
+
+
+def test_selftest_wait_arguments_need_no_gpu(lib):
+    from drafter_sampling_gb300 import _lib
+    fake = ctypes.c_void_p(256)
+    bad = _lib.VT_ERR_INVALID_ARG
+    assert lib.vt_selftest_wait(3, 10, None, fake, None) == bad         # unknown wait
+    assert lib.vt_selftest_wait(-1, 10, None, fake, None) == bad
+    assert lib.vt_selftest_wait(0, 0, None, fake, None) == bad          # limit 0
+    assert lib.vt_selftest_wait(0, (1 << 20) + 1, None, fake, None) == bad
+    assert lib.vt_selftest_wait(2, 10, None, fake, None) == bad         # flag missing
+    assert lib.vt_selftest_wait(0, 10, None, None, None) == bad         # no status word
