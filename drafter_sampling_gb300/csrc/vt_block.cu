@@ -26,7 +26,10 @@ size_t draft_ws(const vt_block_desc& d) {
   return align_up(vt_draft_workspace_bytes(d.B, d.H, d.K), 256);
 }
 
-// the kernels of one block, on stream s
+// the kernels of one block, on stream s.  The hidden states are inputs of
+// the block: no kernel of it writes them, and a graph launch starts only
+// after everything earlier in its stream has completed, so every projection
+// may stage them before its dependency wait (hidden_ready).
 int record_block(const vt_block_desc& d, cudaStream_t s) {
   char* ws = static_cast<char*>(d.workspace);
   const size_t dws = draft_ws(d);
@@ -35,7 +38,7 @@ int record_block(const vt_block_desc& d, cudaStream_t s) {
         d.hidden + (size_t)j * d.B * d.H, d.B, d.H, d.W_trim, d.trim_ids, d.K,
         d.u_draft != nullptr ? d.u_draft + (size_t)j * d.B : nullptr, d.temperature,
         d.q + (size_t)j * d.K, (int64_t)d.gamma * d.K, d.draft_tokens + j, d.gamma,
-        d.dev_status, ws, dws, s, j == 0 ? 1 : 0);
+        d.dev_status, ws, dws, s, j == 0 ? 1 : 0, 1);
     if (st != VT_OK) return st;
   }
   return vt_verify(d.target_logits, d.logits_dtype, d.B, d.gamma, d.V, d.q, d.inv_map, d.K,

@@ -879,7 +879,7 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
 // z = out_scale * hidden @ W^T on the tensor cores; part[tile][b] partials
 int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
-                int* status, int status_reset, int greedy, int* groups_out) {
+                int* status, int status_reset, int greedy, int hidden_ready, int* groups_out) {
   const int BN = (B <= 16) ? 16 : (B <= 32) ? 32 : (B <= 64) ? 64 : (B <= 128) ? 128 : 256;
   CUtensorMap mw, mh;
   if (!make_bf16_map(&mw, W, (uint64_t)K, (uint64_t)H, umma::kBM)) return VT_ERR_CUDA;
@@ -898,6 +898,7 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   a.status_reset = status_reset;
   a.stages = 2;
   a.greedy = greedy;
+  a.hidden_ready = hidden_ready;
   const int tiles = (K + umma::kBM - 1) / umma::kBM;
   *groups_out = tiles;
   // wide batches: two tiles per CTA share each staged block of hidden states
@@ -911,14 +912,16 @@ int launch_umma(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint
   }
 }
 
-// the projection through whichever engine the shapes allow
+// the projection through whichever engine the shapes allow; hidden_ready:
+// no kernel still running writes the hidden states (see HeadArgs)
 int launch_head(cudaStream_t s, const uint16_t* hidden, int B, int H, const uint16_t* W, int K,
                 float out_scale, float* out, int64_t ldo, float2* part, int* zero_ints, int nzero,
-                int* status, int status_reset, int greedy, int* groups_out, int* tile_rows_out) {
+                int* status, int status_reset, int greedy, int* groups_out, int* tile_rows_out,
+                int hidden_ready = 0) {
   if (umma_supported(hidden, B, H, W)) {
     *tile_rows_out = umma::kBM;
     return launch_umma(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero, status,
-                       status_reset, greedy, groups_out);
+                       status_reset, greedy, hidden_ready, groups_out);
   }
   *tile_rows_out = kGemvRowTile;
   return launch_gemv(s, hidden, B, H, W, K, out_scale, out, ldo, part, zero_ints, nzero,
@@ -967,14 +970,15 @@ extern "C" int vt_draft_step(const uint16_t* hidden, int32_t B, int32_t H,
                              void* workspace, size_t workspace_bytes, void* stream) {
   return vt::draft_step_impl(hidden, B, H, W_trim, trim_ids, K, uniforms, temperature, q, ldq,
                              tokens, ld_tokens, dev_status, workspace, workspace_bytes, stream,
-                             1);
+                             1, 0);
 }
 
 int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint16_t* W_trim,
                         const int32_t* trim_ids, int32_t K, const float* uniforms,
                         float temperature, float* q, int64_t ldq, int32_t* tokens,
                         int64_t ld_tokens, int32_t* dev_status, void* workspace,
-                        size_t workspace_bytes, void* stream, int status_reset) {
+                        size_t workspace_bytes, void* stream, int status_reset,
+                        int hidden_ready) {
   using namespace vt;
   int st = check_draft_args(hidden, B, H, W_trim, K, temperature, true);
   if (st != VT_OK) return st;
@@ -993,7 +997,7 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
   int grid = 0, tile_rows = 0;
   st = launch_head(s, hidden, B, H, W_trim, K, greedy ? 1.0f : VT_LOG2E / temperature, q, ldq,
                    ws.part, nullptr, 0, dev_status, status_reset, greedy ? 1 : 0, &grid,
-                   &tile_rows);
+                   &tile_rows, hidden_ready);
   if (st != VT_OK) return st;
   if (greedy) {
     GreedyFinArgs ga;

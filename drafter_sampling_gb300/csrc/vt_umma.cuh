@@ -15,7 +15,9 @@
 //
 // The first ring stages of W_trim are requested before the kernel waits on
 // the previous kernel in the stream (programmatic dependent launch); the
-// hidden states and all outputs come after that wait.
+// hidden states come after that wait unless the caller knows that no kernel
+// still running writes them (the drafting steps of a captured block), and
+// all outputs always do.
 //
 // Every wait on an mbarrier is bounded: on expiry the kernel records
 // VT_DEV_TIMEOUT, drains its own TMA copies (bounded), frees its tensor memory
@@ -184,6 +186,8 @@ struct HeadArgs {
   int status_reset;
   int stages;
   int greedy;        // part holds (max z, its lowest row) instead of (max, sum 2^(z-max))
+  int hidden_ready;  // the hidden states were complete before the previous kernel in the
+                     // stream started: they may be staged before the dependency wait
 };
 
 // (value, index) pairs of an argmax, ties to the lower index; a NaN value
@@ -262,8 +266,10 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   // fills the first stages with W_trim tiles before waiting on it: W_trim is
   // a weight, never written by the kernel just before this one (the kernels
   // of this library release their dependents only after their own wait, so
-  // every older kernel has completed).  Everything else -- the hidden states
-  // and every output -- waits for the previous kernel (griddepcontrol.wait).
+  // every older kernel has completed).  The hidden states join them when the
+  // caller says no running kernel writes them (hidden_ready).  Everything
+  // else -- every output -- waits for the previous kernel
+  // (griddepcontrol.wait).
   if (warp == 0 && lane == 0) {
     // TMA producer
     const int pre = min(S, nk);
@@ -273,11 +279,15 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
       for (int t = 0; t < TM; ++t)
         tma_load_2d(smem + (size_t)kb * stage_bytes + t * kABytes, &map_w,
                     ((kb + rot) % nk) * kBK, m0 + t * kBM, &full_bar[kb]);
+      if (a.hidden_ready)
+        tma_load_2d(smem + (size_t)kb * stage_bytes + kAB, &map_h, ((kb + rot) % nk) * kBK, 0,
+                    &full_bar[kb]);
     }
     griddep_wait();
-    for (int kb = 0; kb < pre; ++kb)
-      tma_load_2d(smem + (size_t)kb * stage_bytes + kAB, &map_h, ((kb + rot) % nk) * kBK, 0,
-                  &full_bar[kb]);
+    if (!a.hidden_ready)
+      for (int kb = 0; kb < pre; ++kb)
+        tma_load_2d(smem + (size_t)kb * stage_bytes + kAB, &map_h, ((kb + rot) % nk) * kBK, 0,
+                    &full_bar[kb]);
     int issued = pre;
     bool ok = true;
     for (int kb = pre; kb < nk && ok; ++kb) {
