@@ -118,3 +118,26 @@ def test_drafting_flags_of_every_step_are_kept(vt):
     torch.cuda.synchronize()
     assert int(g.dev_status[0].item()) & vt.VT_DEV_NONFINITE
     g.close()
+
+
+def test_hidden_states_written_just_before_a_replay_are_read(vt):
+    # the projections of a replay stage the hidden states before their
+    # dependency wait: a kernel that rewrites them right before the launch, on
+    # the same stream and with no synchronisation between, must still be seen
+    x = _inputs(8, 3, 256, 1024, 4000, seed=6)
+    g = _graph(vt, x, 1.0)
+    g.launch()
+    torch.cuda.synchronize()
+    first = g.draft_tokens.clone()
+    fresh = _dev(synthetic.hidden_states(tuple(x["hidden"].shape), seed=77).view(np.int16))
+    big = torch.empty(1 << 26, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        big.mul_(1.0)                          # keep the stream busy before the rewrite
+    x["hidden"].copy_(fresh)
+    g.launch()
+    torch.cuda.synchronize()
+    ref = _direct(vt, x, 1.0)
+    assert _same(g.q, ref[0]) and torch.equal(g.draft_tokens, ref[1])
+    assert torch.equal(g.out_tokens, ref[2])
+    assert not torch.equal(g.draft_tokens, first)
+    g.close()
