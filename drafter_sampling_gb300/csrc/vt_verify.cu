@@ -31,9 +31,10 @@
 // bit-identical in both places.
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "vt_common.cuh"
+#include "vt_internal.h"
+#include "vt_verify_common.cuh"
 
 namespace vt {
 namespace {
@@ -44,55 +45,6 @@ constexpr int kResPerThread = 8;      // residual ids per thread
 constexpr int kResChunk = kNT * kResPerThread;
 constexpr int kStatsBytes = 32768;    // bytes of logits per stats item
 constexpr int kMaxChunks1 = 64;
-
-template <typename T> struct Elem;
-template <> struct Elem<float> {
-  static constexpr int kVec = 4;  // elements per 16-byte load
-  __device__ static float load(const float* p) { return __ldg(p); }
-  __device__ static void unpack16(uint4 v, float* x) {
-    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
-    x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
-  }
-  // eight consecutive elements at a 32-byte aligned index
-  __device__ static void load8(const float* p, float* x) {
-    const uint4* q = reinterpret_cast<const uint4*>(p);
-    unpack16(__ldg(q), x);
-    unpack16(__ldg(q + 1), x + 4);
-  }
-};
-template <> struct Elem<uint16_t> {
-  static constexpr int kVec = 8;
-  __device__ static float load(const uint16_t* p) { return bf16_bits_to_float(__ldg(p)); }
-  __device__ static void unpack16(uint4 v, float* x) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[2 * k] = __uint_as_float(w[k] << 16);
-      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-  }
-  __device__ static void load8(const uint16_t* p, float* x) {
-    unpack16(__ldg(reinterpret_cast<const uint4*>(p)), x);
-  }
-};
-
-template <int N>
-__device__ __forceinline__ void online_update(float& m, float& s, const float* x, float scale) {
-  float t[N];
-  float vmax = kNegBig;
-#pragma unroll
-  for (int k = 0; k < N; ++k) {
-    t[k] = x[k] * scale;
-    vmax = fmaxf(vmax, t[k]);
-  }
-  if (vmax > m) {
-    s *= exp2_approx(m - vmax);
-    m = vmax;
-  }
-#pragma unroll
-  for (int k = 0; k < N; ++k) s += exp2_approx(t[k] - m);
-}
-
 
 struct VArgs {
   const void* logits;
@@ -808,6 +760,30 @@ int launch_verify_tree(const VArgs& a, const TreeArgs& t, cudaStream_t s) {
 }  // namespace
 }  // namespace vt
 
+namespace vt {
+namespace {
+
+// Host-checkable argument errors of vt_verify (and vt_verify_noalloc).
+int verify_check_args(const void* target_logits, int32_t logits_dtype, int32_t B, int32_t gamma,
+                      int32_t V, const float* q, const int32_t* inv_map, int32_t K,
+                      const int32_t* draft_tokens, const float* u_accept,
+                      const float* u_resample, float temperature, const int32_t* out_tokens,
+                      const int32_t* out_num_accepted, const int32_t* dev_status) {
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !dev_status)
+    return VT_ERR_INVALID_ARG;
+  if (!greedy && (!q || !inv_map || !u_accept || !u_resample)) return VT_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || gamma < 1 || gamma > kMaxGamma || V < 1 || K < 1 || K > V ||
+      V > (1 << 22))
+    return VT_ERR_INVALID_ARG;
+  if (logits_dtype != VT_F32 && logits_dtype != VT_BF16) return VT_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return VT_ERR_INVALID_ARG;
+  return VT_OK;
+}
+
+}  // namespace
+}  // namespace vt
+
 extern "C" size_t vt_verify_workspace_bytes(int32_t B, int32_t gamma, int32_t V, int32_t K) {
   (void)K;
   if (B < 1 || gamma < 1 || V < 1) return 0;
@@ -823,14 +799,10 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
   using namespace vt;
   // temperature 0: greedy verification (q, inv_map and the uniforms are not read)
   const bool greedy = temperature == 0.f;
-  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !dev_status)
-    return VT_ERR_INVALID_ARG;
-  if (!greedy && (!q || !inv_map || !u_accept || !u_resample)) return VT_ERR_INVALID_ARG;
-  if (B < 1 || B > 65535 || gamma < 1 || gamma > kMaxGamma || V < 1 || K < 1 || K > V ||
-      V > (1 << 22))
-    return VT_ERR_INVALID_ARG;
-  if (logits_dtype != VT_F32 && logits_dtype != VT_BF16) return VT_ERR_INVALID_ARG;
-  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return VT_ERR_INVALID_ARG;
+  const int arg = verify_check_args(target_logits, logits_dtype, B, gamma, V, q, inv_map, K,
+                                    draft_tokens, u_accept, u_resample, temperature, out_tokens,
+                                    out_num_accepted, dev_status);
+  if (arg != VT_OK) return arg;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return VT_ERR_WORKSPACE;
   const VerifyLayout L = verify_layout(B, gamma, V);
   if (workspace_bytes < L.bytes) return VT_ERR_WORKSPACE;
@@ -891,28 +863,23 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
 namespace vt {
 namespace {
 
-constexpr int kNoallocMaxDevices = 64;
-
 // 2 MiB of scratch per device, resident for the life of the process.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[VT_VERIFY_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device.  Host code only
-// holds a stand-in for the symbol, so the address is looked up once per
-// device (with that device current) and cached.
+// Device address of g_noalloc_scratch in the calling thread's current
+// context.  Host code only holds a stand-in for the symbol, and each context
+// that loads the library gets its own copy of the array, so the address is
+// looked up on every call: a cached address would outlive the context it
+// belongs to (cudaDeviceReset, or a caller that switches to a context of its
+// own on the same device).  The lookup is a host-side table query, not a
+// stream operation.
 int noalloc_scratch_address(void** out) {
-  static std::mutex mu;
-  static void* addr[kNoallocMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return VT_ERR_CUDA;
-  if (dev < 0 || dev >= kNoallocMaxDevices) return VT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return VT_ERR_CUDA;
-    addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return VT_ERR_CUDA;
   }
-  *out = addr[dev];
+  *out = p;
   return VT_OK;
 }
 
@@ -927,14 +894,14 @@ extern "C" int vt_verify_noalloc(const void* target_logits, int32_t logits_dtype
                                  int32_t* out_num_accepted, float* out_accept_prob,
                                  int32_t* dev_status, void* stream) {
   using namespace vt;
-  if (B < 1 || gamma < 1 || gamma > kMaxGamma) return VT_ERR_INVALID_ARG;
+  // the argument checks of vt_verify come first, so a bad argument reports
+  // VT_ERR_INVALID_ARG here too; only a valid problem can exceed the scratch
+  const int arg = verify_check_args(target_logits, logits_dtype, B, gamma, V, q, inv_map, K,
+                                    draft_tokens, u_accept, u_resample, temperature, out_tokens,
+                                    out_num_accepted, dev_status);
+  if (arg != VT_OK) return arg;
   const size_t need = vt_verify_workspace_bytes(B, gamma, V, K);
   if (need > VT_VERIFY_NOALLOC_SCRATCH_BYTES) return VT_ERR_SCRATCH_LIMIT;
-  // temperature 0: greedy verification (q, inv_map and the uniforms are not read)
-  const bool greedy = temperature == 0.f;
-  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !dev_status)
-    return VT_ERR_INVALID_ARG;
-  if (!greedy && (!q || !inv_map || !u_accept || !u_resample)) return VT_ERR_INVALID_ARG;
   void* scratch = nullptr;
   const int st = noalloc_scratch_address(&scratch);
   if (st != VT_OK) return st;

@@ -297,10 +297,16 @@ int vt_verify(const void* target_logits, int32_t logits_dtype,
  *    larger than VT_VERIFY_NOALLOC_SCRATCH_BYTES is rejected with
  *    VT_ERR_SCRATCH_LIMIT before any device work (about 3800 rows
  *    B*(gamma+1) fit, e.g. B=256 with gamma=8).
- *  - Set-up: the first call on each device looks up the array's device
- *    address (cudaGetSymbolAddress) with that device current, and returns
- *    VT_ERR_CUDA if the lookup fails.  Make that first call before any
- *    stream capture.
+ *  - Set-up: every call looks up the array's device address
+ *    (cudaGetSymbolAddress) in the calling thread's current context and
+ *    returns VT_ERR_CUDA if the lookup fails.  Each context that loads the
+ *    library has its own copy of the array, so no address is cached: a
+ *    call after cudaDeviceReset, or from a context the caller created and
+ *    made current itself, uses that context's copy.  The first call in a
+ *    context also loads the library's device code there; make it before
+ *    any stream capture.
+ *  - Arguments are checked exactly as vt_verify checks them (same codes);
+ *    the scratch limit is checked after that.
  *  - Sharing: every call on a device uses the same array, which keeps what
  *    the last call left in it; the kernels clear what must start at zero.
  *    Calls that can overlap on the GPU (e.g. on two streams with no ordering

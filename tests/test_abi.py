@@ -198,3 +198,25 @@ def test_selftest_wait_arguments_need_no_gpu(lib):
     assert lib.vt_selftest_wait(0, (1 << 20) + 1, None, fake, None) == bad
     assert lib.vt_selftest_wait(2, 10, None, fake, None) == bad         # flag missing
     assert lib.vt_selftest_wait(0, 10, None, None, None) == bad         # no status word
+
+
+def test_noalloc_checks_arguments_before_its_scratch_limit(lib):
+    from drafter_sampling_gb300 import _lib
+    fake = ctypes.c_void_p(256)
+    bad = _lib.VT_ERR_INVALID_ARG
+    # out-of-range arguments report what vt_verify reports, not the scratch limit
+    for B, gamma, V, K, dt, T in [(70000, 6, 1000, 10, _lib.VT_F32, 1.0),
+                                  (16, 65, 1000, 10, _lib.VT_F32, 1.0),
+                                  (16, 6, (1 << 22) + 1, 10, _lib.VT_F32, 1.0),
+                                  (16, 6, 1000, 1001, _lib.VT_F32, 1.0),
+                                  (16, 6, 1000, 10, 7, 1.0),
+                                  (16, 6, 1000, 10, _lib.VT_F32, -1.0),
+                                  (16, 6, 1000, 10, _lib.VT_F32, float("nan"))]:
+        args = (fake, dt, B, gamma, V, fake, fake, K, fake, fake, fake, T, fake, fake, None,
+                fake, None)
+        assert lib.vt_verify_noalloc(*args) == bad, (B, gamma, V, K, dt, T)
+        assert lib.vt_verify(*args[:-1], fake, 1 << 30, None) == bad, (B, gamma, V, K, dt, T)
+    # a missing pointer too
+    st = lib.vt_verify_noalloc(fake, _lib.VT_F32, 16, 6, 1000, None, fake, 10, fake, fake, fake,
+                               1.0, fake, fake, None, fake, None)
+    assert st == bad
