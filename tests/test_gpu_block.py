@@ -1,7 +1,8 @@
 """The speculative block as a CUDA graph (vt_block_graph_*): a replay gives
 bit-for-bit what the same vt_draft_step / vt_verify calls give when made
-directly (those calls are compared with the oracle in their own tests), it
-reads the input buffers live, and the greedy block works the same way."""
+directly, a replay matches the oracle's block (drafting and verification) on
+the same generator inputs, it reads the input buffers live, and the greedy
+block works the same way."""
 import numpy as np
 import pytest
 
@@ -140,4 +141,74 @@ def test_hidden_states_written_just_before_a_replay_are_read(vt):
     assert _same(g.q, ref[0]) and torch.equal(g.draft_tokens, ref[1])
     assert torch.equal(g.out_tokens, ref[2])
     assert not torch.equal(g.draft_tokens, first)
+    g.close()
+
+
+def _oracle_block(x, T, dtype):
+    """The block on the oracle: each drafting step from the same hidden
+    states, trimmed head and uniforms, then the verification of the GPU's
+    drafted tokens (equal to the oracle's wherever a draw is not a boundary
+    case, and then checked as a valid draw) with the oracle's own q."""
+    import oracle
+    h = x["hidden"].cpu().numpy().view(np.uint16)
+    W = x["W_trim"].cpu().numpy().view(np.uint16)
+    trim_ids = x["trim_ids"].cpu().numpy()
+    u = x["u_draft"].cpu().numpy()
+    gamma, B, _ = h.shape
+    steps = [oracle.draft_step(h[j], W, trim_ids, u[j], T) for j in range(gamma)]
+    logits = x["logits"].cpu()
+    logits = logits.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else logits.numpy()
+    return steps, logits
+
+
+@pytest.mark.parametrize("B,gamma,H,K,V,T,dtype", [
+    (16, 6, 2048, 32768, 128256, 1.0, "f32"),   # the block of the bench step
+    (8, 4, 1024, 6000, 40000, 0.7, "bf16"),     # bf16 target logits, T = 0.7
+])
+def test_graph_replay_against_the_oracle(vt, B, gamma, H, K, V, T, dtype):
+    # one replay of the captured block (VocabTrim Appendix C.1, Algorithm 2:
+    # draft gamma tokens, then score and verify them) against the oracle run
+    # on the same generator inputs
+    import oracle
+    from parity import BOUNDARY, assert_probs_close, compare_verify, draw_is_valid
+    x = _inputs(B, gamma, H, K, V, seed=3 * B + gamma, dtype=dtype)
+    g = _graph(vt, x, T)
+    g.launch()
+    torch.cuda.synchronize()
+    assert int(g.dev_status[0].item()) == 0 and int(g.dev_status[1].item()) == 0
+    steps, logits = _oracle_block(x, T, dtype)
+    q = g.q.cpu().numpy()
+    tok = g.draft_tokens.cpu().numpy()
+    trim_ids = x["trim_ids"].cpu().numpy()
+    pos = {int(t): j for j, t in enumerate(trim_ids)}
+    compared = 0
+    for j, ref in enumerate(steps):
+        assert_probs_close(q[:, j, :], ref["q"], f"q of drafting step {j}")
+        for b in range(B):
+            if ref["margin"][b] > BOUNDARY:
+                assert tok[b, j] == ref["tokens"][b], (j, b)
+                compared += 1
+            else:
+                assert draw_is_valid(ref["q"][b], x["u_draft"][j, b].item(), pos[int(tok[b, j])])
+    assert compared >= (B * gamma) // 3
+    q_ref = np.stack([s["q"] for s in steps], axis=1)
+    ref = oracle.verify(logits, q_ref, x["inv_map"].cpu().numpy(), tok,
+                        x["u_accept"].cpu().numpy(), x["u_resample"].cpu().numpy(), T,
+                        logits_dtype=dtype)
+
+    im = x["inv_map"].cpu().numpy()
+
+    def weights(b, n):
+        l = oracle.bf16_to_f64(logits[b, n]) if dtype == "bf16" else logits[b, n]
+        p = oracle.softmax(l, T)
+        if n < gamma:
+            qf = np.zeros(V)
+            qf[im >= 0] = q_ref[b, n, im[im >= 0]]
+            p = oracle.residual_weights(p, qf)
+        return p, float(x["u_resample"][b, n].item())
+
+    stats = compare_verify(g.out_tokens.cpu().numpy(), g.out_num_accepted.cpu().numpy(),
+                           g.out_accept_prob.cpu().numpy(), ref, draw_weights=weights)
+    assert stats["compared"] + stats["excluded_seq"] == B
+    assert stats["compared"] >= B // 2
     g.close()

@@ -99,7 +99,11 @@ def test_draft_step_trimmed_head_full_size(vt, B):
     perm = synthetic.rank_permutation(128256)
     _, trim_ids, _ = synthetic.trimmed_set(128256, 32768, perm)
     u = synthetic.uniforms(50 + B, 1, B)
-    _check_step(vt, hidden, W, trim_ids, u, 1.0)
+    checked = _check_step(vt, hidden, W, trim_ids, u, 1.0)
+    # q's bins here are about 1/32768 = 3e-5 wide against a boundary band 2e-5
+    # wide, so about half the draws are compared exactly (on these seeds:
+    # 1 of 1, 5 of 8, 9 of 16, 33 of 64); the rest are checked as valid draws
+    assert checked >= max(1, B // 2)
 
 
 def test_draft_step_large_batch_full_size(vt):
@@ -128,7 +132,10 @@ def test_full_vocab_head_and_trimmed_consistency(vt):
     W = synthetic.normal_bf16(g, (V, H), 0.02)
     u = synthetic.uniforms(60, 1, B)
     ident = np.arange(V, dtype=np.int32)
-    _check_step(vt, hidden, W, ident, u, 1.0)
+    checked = _check_step(vt, hidden, W, ident, u, 1.0)
+    # bins of about 1/128256 = 7.8e-6 against a band 2e-5 wide: about a third
+    # of the draws are compared exactly (3 of 8 on this seed)
+    assert checked >= B // 4
     perm = synthetic.rank_permutation(V)
     _, trim_ids, _ = synthetic.trimmed_set(V, K, perm)
     qf, _, _ = vt.vt_draft_step(_bf(hidden), _bf(W), _dev(ident), _dev(u), 1.0)
