@@ -311,87 +311,118 @@ class GpuStep:
 
 
 # ------------------------------------------------- the oracle on the host
-def oracle_sample(host: HostInputs, k: int):
-    """Time the CPU oracle on sample k of every row; returns per-row seconds
-    scaled to one full step (the sample fraction of each row is stated)."""
+def oracle_step(x, draft_steps: int = GAMMA):
+    """One step of the hot path on the CPU oracle, on the step's own inputs:
+    the 50M-id histogram and Top-K, the trim, `draft_steps` drafting steps of
+    B = 16 rows over the full trimmed head, and the verification of all 16
+    sequences.  Returns seconds per row."""
     import oracle
-    out = {}
-    n_s = N_CAL // 512
-    lo = (k % 512) * n_s
+    t = {}
     t0 = time.perf_counter()
-    counts = oracle.token_histogram(host.ids[lo:lo + n_s], V)
+    topk = oracle.top_k(oracle.token_histogram(x["ids"], V), K)
     t1 = time.perf_counter()
-    topk = oracle.top_k(counts, K)
+    W_trim, trim_ids, inv_map = oracle.trim_head(x["W"], topk)
     t2 = time.perf_counter()
-    out["calibrate"] = (t1 - t0) * 512 + (t2 - t1)
-    kk = K // 64
-    W_trim, trim_ids, inv_map = oracle.trim_head(host.W, topk[:kk])
+    q = np.zeros((B, GAMMA, K))
+    tokens = np.zeros((B, GAMMA), dtype=np.int32)
+    for j in range(GAMMA):
+        if j < draft_steps:
+            d = oracle.draft_step(x["hidden"][j], W_trim, trim_ids, x["u_draft"][j], T)
+            q[:, j, :], tokens[:, j] = d["q"], d["tokens"]
+        else:  # the remaining positions reuse the first drafted q and tokens
+            q[:, j, :], tokens[:, j] = q[:, 0, :], tokens[:, 0]
     t3 = time.perf_counter()
-    out["trim"] = (t3 - t2) * 64
-    b = k % B
-    j = k % GAMMA
-    sl = slice(b, b + 1)
-    d = oracle.draft_step(host.hidden[j][sl], W_trim, trim_ids, host.u_draft[j][sl], T)
+    oracle.verify(x["logits"], q, inv_map, tokens, x["u_accept"], x["u_resample"], T)
     t4 = time.perf_counter()
-    out["draft"] = (t4 - t3) * B * (K / kk) * GAMMA
-    # verify one sequence with a q built over the sample's trimmed set
-    q = np.zeros((1, GAMMA, kk))
-    q[:, :, :] = d["q"][0]
-    draft = np.repeat(d["tokens"][None, :], GAMMA, axis=1)
-    t5 = time.perf_counter()
-    oracle.verify(host.logits[sl], q, inv_map, draft, host.u_accept[sl], host.u_resample[sl], T)
-    t6 = time.perf_counter()
-    out["verify"] = (t6 - t5) * B
+    return {"calibrate": t1 - t0, "trim": t2 - t1, "draft": (t3 - t2) / draft_steps,
+            "verify": t4 - t3}
+
+
+def oracle_child(path: str, mode: str, runs: int) -> int:
+    """Entry of the spawned process that times the oracle on the step's
+    inputs (saved by the parent as .npy files in `path`); prints one JSON
+    line with the per-run row seconds."""
+    x = {n: np.load(os.path.join(path, n + ".npy"), mmap_mode="r")
+         for n in ("ids", "W", "hidden", "u_draft", "logits", "u_accept", "u_resample")}
+    x = {n: np.ascontiguousarray(v) for n, v in x.items()}
+    steps = GAMMA if mode == "all" else 1
+    oracle_step(x, steps)  # warm-up
+    out = [oracle_step(x, steps) for _ in range(runs)]
+    print(json.dumps({"runs": out, "cpu_count": os.cpu_count()}))
+    return 0
+
+
+ORACLE_THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
+                      "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def cpu_baseline_measure(host: HostInputs, runs: int = 5):
+    """The oracle as it stands, timed on whole rows of the step's own inputs
+    in child processes: once with every host core available (numpy's BLAS
+    threads; the histogram and the verification loop are single-threaded
+    numpy) and once pinned to one thread.  Medians of `runs` runs."""
+    import tempfile
+    inp = host.step_inputs()
+    inp["W"] = host.W
+    res = {}
+    with tempfile.TemporaryDirectory() as d:
+        for n, v in inp.items():
+            np.save(os.path.join(d, n + ".npy"), np.ascontiguousarray(v))
+        for mode in ("all", "one"):
+            env = {k: v for k, v in os.environ.items() if k not in ORACLE_THREAD_VARS}
+            if mode == "one":
+                env.update({k: "1" for k in ORACLE_THREAD_VARS})
+            r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-child", d,
+                                "--oracle-mode", mode, "--oracle-runs", str(runs)],
+                               capture_output=True, text=True, env=env, timeout=900)
+            if r.returncode != 0:
+                raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
+            res[mode] = json.loads(r.stdout.strip().splitlines()[-1])
+    out = {}
+    for mode, d in res.items():
+        rows = {r: statistics.median([x[r] for x in d["runs"]]) for r in ROWS}
+        per_step = rows["calibrate"] + rows["trim"] + GAMMA * rows["draft"] + rows["verify"]
+        out[mode] = {"rows_s": rows, "s_per_step": per_step, "cpu_count": d["cpu_count"],
+                     "runs": len(d["runs"])}
     return out
 
 
-ORACLE_SAMPLE_TEXT = ("per sample: histogram of 1/512 of the 50M ids (x512) + full Top-K; "
-                      "trim of 1/64 of the K rows (x64); one drafter row of one position over "
-                      "the 1/64 trimmed head (x B*gamma*64); one verified sequence (x B); "
-                      "numpy fp64 oracle")
-
-
-def run_oracle_for(seconds: float, host: HostInputs, max_samples=None):
-    t_start = time.time()
-    c0 = time.process_time()
-    tot = {r: 0.0 for r in ROWS}
-    n = 0
-    while time.time() - t_start < seconds and (max_samples is None or n < max_samples):
-        s = oracle_sample(host, n)
-        for r in ROWS:
-            tot[r] += s[r]
-        n += 1
-    wall = time.time() - t_start
-    cpu = time.process_time() - c0
-    per_step = sum(tot.values()) / n
-    return n, per_step, wall, max(1, round(cpu / wall)), {r: tot[r] / n for r in ROWS}
+def config_dict(world: int):
+    """The workload of one step, identical in both arms' lines."""
+    return {"workload": workload_text(), "global_batch": B * world, "seq_len": GAMMA + 1,
+            "parallelism": f"replicas x{world}",
+            "l2": "each step streams >1.3 GB (>4x L2) of distinct inputs; logits rotate over "
+                  "2 buffers"}
 
 
 def run_reference(args):
+    """The oracle as the reference arm: every step is one full step of the
+    hot path on the CPU oracle (no sampling, no extrapolation), on every host
+    core numpy's BLAS uses; rank 0 alone runs it."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     host = HostInputs()
-    for k in range(args.warmup):
-        oracle_sample(host, k)
-    tot = 0.0
-    c0 = time.process_time()
-    t0 = time.time()
-    for k in range(args.steps):
-        tot += sum(oracle_sample(host, k).values())
-    wall = time.time() - t0
-    cpu = time.process_time() - c0
-    per_step = tot / args.steps
-    value = B * GAMMA / per_step
+    x = dict(host.step_inputs(), W=host.W)
+    for _ in range(args.warmup):
+        oracle_step(x)
+    t0 = time.perf_counter()
+    per = [oracle_step(x) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    value = whole_job_value(args.steps, 1, wall * 1e3)
+    rows = {r: statistics.median([p[r] for p in per]) for r in ROWS}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_text(), "global_batch": B, "seq_len": GAMMA + 1,
-                       "parallelism": "replicas"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": max(1, round(cpu / wall)),
+            "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle",
-                             "sample": f"{args.steps} samples; " + ORACLE_SAMPLE_TEXT},
+                             "sample": f"{args.steps} full steps of the workload timed back to "
+                                       "back (50M-id histogram and Top-K, trim, 6 drafting "
+                                       "steps of 16 rows, verification of 16 sequences), numpy "
+                                       "fp64, BLAS on all cores",
+                             "median_row_s": rows},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -404,6 +435,52 @@ def workload_text():
             "verify B=16 gamma=6 fp32 logits N(0,2)+3 ln Zipf_1.1 rank bias, T=1")
 
 
+def run_row(torch, vt, dev, host, args):
+    """Profiling mode: one full step (it fills W_trim, q, the drafts and the
+    inverse map), then only `args.row`'s calls for warmup + steps iterations,
+    in a process that holds one set of the step's buffers (~1.6 GB).  Made for
+    ncu captures of one kernel (-k, -s 1 skips the set-up step's launch)."""
+    step = GpuStep(torch, vt, dev, host, nsets=1)
+    step.run(0)
+    torch.cuda.synchronize()
+    s = step.vsets[0]
+    calls = {
+        "calibrate": lambda: vt.vt_calibrate_topk(step.ids, V, K, counts=step.counts,
+                                                  topk_ids=step.topk,
+                                                  dev_status=step.status[0:1],
+                                                  workspace=step.ws_cal),
+        "trim": lambda: vt.vt_trim_head(step.W, step.topk, W_trim=step.W_trim,
+                                        trim_ids=step.trim_ids, inv_map=step.inv_map,
+                                        dev_status=step.status[1:2], workspace=step.ws_trim),
+        "draft": lambda: [vt.vt_draft_step(step.hidden[j], step.W_trim, step.trim_ids,
+                                           step.u_draft[j], T, q=step.q[:, j, :],
+                                           tokens=step.tokens[:, j],
+                                           dev_status=step.status[2:3],
+                                           workspace=step.ws_draft) for j in range(GAMMA)],
+        "verify": lambda: vt.vt_verify(s["logits"], step.q, step.inv_map, step.tokens,
+                                       s["u_acc"], s["u_res"], T, out_tokens=step.out_tokens,
+                                       out_num_accepted=step.out_n,
+                                       out_accept_prob=step.out_acc,
+                                       dev_status=step.status[3:4], workspace=step.ws_ver),
+    }
+    fn = calls[args.row]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    per_call = e0.elapsed_time(e1) * 1e3 / (args.steps * CALLS_PER_STEP[args.row])
+    print(json.dumps({"row": args.row, "calls": args.steps * CALLS_PER_STEP[args.row],
+                      "us_per_call": per_call,
+                      "dev_status": [int(v) for v in step.status.cpu().tolist()]}))
+    return 0
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -414,7 +491,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--row", default=None, choices=ROWS,
+                    help="profiling mode: after one full step, run only this row's calls for "
+                         "warmup + steps iterations (prints a short summary, not the bench line)")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-mode", default="all", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-runs", type=int, default=5, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        return oracle_child(args.oracle_child, args.oracle_mode, args.oracle_runs)
     if args.impl == "reference":
         return run_reference(args)
 
@@ -432,6 +517,8 @@ def main():
     import drafter_sampling_gb300 as vt
 
     host = HostInputs()
+    if args.row:
+        return run_row(torch, vt, dev, host, args)
     # every step streams ~1.3 GB (ids, W, W_trim, logits), far more than L2,
     # so no input is L2-resident when the next step reads it; the logits also
     # rotate between two buffers
@@ -511,10 +598,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_text(), "global_batch": B * world, "seq_len": GAMMA + 1,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "each step streams >1.3 GB (>4x L2) of distinct inputs; logits "
-                         "rotate over 2 buffers"},
+        "config": config_dict(world),
         "roofline": {"bound": "hbm", "kernel": f"vt_{dominant} (dominant row)",
                      "achieved": dom["achieved_gbs"], "peak": peak, "unit": "GB/s",
                      "frac": dom["achieved_gbs"] / peak, "traffic": dom["traffic"],
@@ -543,14 +627,25 @@ def main():
             "calibration_H3072": run_calibration_h3072(torch, vt, step, peak),
             "large_batch_B256": run_large_batch(torch, vt, step, peak, peak_tf)}
 
+    line["timing_distribution"] = run_timing_distribution(torch, vt, step, host)
     if not args.no_e2e:
         line["e2e"] = run_e2e(torch, step, host, stream, args, dist, dev, world)
+        line["e2e_online_block"] = run_e2e_block(torch, step, host, stream, args, dist, dev,
+                                                 world)
     if rank == 0 and not args.no_cpu_baseline:
-        n, per_step, wall, cores, per_row = run_oracle_for(12.0, host)
-        line["cpu_baseline"] = {"value": B * GAMMA / per_step, "unit": UNIT, "cores": cores,
-                                "kind": "oracle",
-                                "sample": f"{n} samples in {wall:.1f} s; " + ORACLE_SAMPLE_TEXT,
-                                "est_s_per_step": per_row}
+        cb = cpu_baseline_measure(host)
+        line["cpu_baseline"] = {
+            "value": B * GAMMA / cb["all"]["s_per_step"], "unit": UNIT,
+            "cores": cb["all"]["cpu_count"], "kind": "oracle",
+            "sample": "whole rows of the step's own inputs, median of 5 runs each: the 50M-id "
+                      "histogram and Top-K, the trim, 6 drafting steps of 16 rows over the full "
+                      "trimmed head, the verification of 16 sequences; numpy fp64 with its "
+                      "BLAS on every host core (histogram and verification loops on one core)",
+            "median_row_s": cb["all"]["rows_s"],
+            "single_thread": {"value": B * GAMMA / cb["one"]["s_per_step"], "unit": UNIT,
+                              "cores": 1, "median_row_s": cb["one"]["rows_s"],
+                              "sample": "the same rows with one BLAS thread; one drafting "
+                                        "step timed per run, counted 6 times per step"}}
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
@@ -938,6 +1033,181 @@ def run_large_batch(torch, vt, step, peak, peak_tf):
                 "dev_status": [int(x) for x in st.cpu().tolist()]})
     del Wt, qd, wsd
     return res
+
+
+def _pcts(xs):
+    xs = np.asarray(xs, dtype=np.float64)
+    return {"median_us": float(np.median(xs)), "p10_us": float(np.percentile(xs, 10)),
+            "p90_us": float(np.percentile(xs, 90)), "n": int(xs.size)}
+
+
+def run_timing_distribution(torch, vt, step, host, ncalls: int = 240):
+    """Per-call time distributions of the two rows the metric and the
+    roofline rest on, over >= 200 launches each.
+    verify: `ncalls` calls on the batched-verify workload, logits rotating
+      over three buffers (172 MB, more than L2), (a) one event pair around
+      every call and (b) CUDA graphs of 20 calls replayed back to back (per
+      call time of each replay);
+    draft: the six drafting calls of a block as in the step, (a) with an
+      event pair around each call, (b) graphs of 20 blocks replayed (per call)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(step.dev)
+    q, draft, inv_map = t(host.q_verify), t(host.draft_verify), t(host.inv_map_verify)
+    logits = [step.vsets[0]["logits"], step.vsets[1]["logits"], step.vsets[0]["logits"].clone()]
+    s0 = step.vsets[0]
+    Ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def ver(k):
+        vt.vt_verify(logits[k % 3], q, inv_map, draft, s0["u_acc"], s0["u_res"], T,
+                     out_tokens=step.out_tokens, out_num_accepted=step.out_n,
+                     out_accept_prob=step.out_acc, dev_status=step.status[3:4],
+                     workspace=step.ws_ver)
+
+    def drf(j):
+        vt.vt_draft_step(step.hidden[j], step.W_trim, step.trim_ids, step.u_draft[j], T,
+                         q=step.q[:, j, :], tokens=step.tokens[:, j],
+                         dev_status=step.status[2:3], workspace=step.ws_draft)
+
+    out = {}
+    for name, fn, per in (("verify", ver, 1), ("draft", drf, GAMMA)):
+        for k in range(6):
+            fn(k % per if per > 1 else k)
+        torch.cuda.synchronize()
+        ev = [(Ev(), Ev()) for _ in range(ncalls)]
+        for k in range(ncalls):
+            ev[k][0].record()
+            fn(k % per if per > 1 else k)
+            ev[k][1].record()
+        torch.cuda.synchronize()
+        each = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        # graphs of 20 calls (verify) or 20 blocks of six calls (draft)
+        gcalls = 20 * per
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for k in range(gcalls):
+                    fn(k % per if per > 1 else k)
+        torch.cuda.synchronize()
+        reps = max(12, -(-ncalls // gcalls))
+        per_call = []
+        for r in range(reps + 2):
+            a, b = Ev(), Ev()
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                per_call.append(a.elapsed_time(b) * 1e3 / gcalls)
+        del g
+        alg = algorithmic_bytes()[name]
+        pk, _ = peaks()
+        e, gr = _pcts(each), _pcts(per_call)
+        out[name] = {"event_pair_per_call": e, "graph_per_call": gr,
+                     "graph_launches": reps * gcalls,
+                     "frac_of_measured_hbm_at_graph_median":
+                         alg / (gr["median_us"] * 1e-6) / 1e9 / pk}
+    out["verify"]["positions_per_s_at_graph_median"] = \
+        B * GAMMA / (out["verify"]["graph_per_call"]["median_us"] * 1e-6)
+    out["note"] = ("event_pair_per_call: one pair of events around each call (the pair itself "
+                   "costs the launch overlap between calls); graph_per_call: replays of a graph "
+                   "of calls, time per call of each replay")
+    return out
+
+
+def run_e2e_block(torch, step, host, stream, args, dist, dev, world):
+    """The online block end to end through the public API: per block the host
+    ships only what a decoder produces per block (the drafter's hidden states
+    and uniforms, the target's logits, the verification uniforms, ~58 MB) and
+    reads the verified tokens back; calibration and trim are offline
+    (VocabTrim section 3) and done once before the timed region, like the
+    trimmed head's weights.  Copies of block k+1 overlap block k."""
+    vt = step.vt
+    inp = host.step_inputs()
+    names = ("hidden", "u_draft", "logits", "u_accept", "u_resample")
+    pinned = {n: torch.from_numpy(np.ascontiguousarray(
+        inp[n].view(np.int16) if inp[n].dtype == np.uint16 else inp[n])).pin_memory()
+        for n in names}
+    sets = [{n: torch.empty(pinned[n].shape, dtype=pinned[n].dtype, device=dev) for n in names}
+            for _ in range(2)]
+    out_host = torch.empty(B * (GAMMA + 1) + B, dtype=torch.int32).pin_memory()
+    nblocks = max(1, min(args.steps, 50))
+    copy_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+
+    def issue_copy(k):
+        x = k % 2
+        copy_stream.wait_event(done[x])
+        with torch.cuda.stream(copy_stream):
+            for n in names:
+                sets[x][n].copy_(pinned[n], non_blocking=True)
+            ready[x].record(copy_stream)
+
+    def run_block(k):
+        x = k % 2
+        d = sets[x]
+        stream.wait_event(ready[x])
+        for j in range(GAMMA):
+            vt.vt_draft_step(d["hidden"][j], step.W_trim, step.trim_ids, d["u_draft"][j], T,
+                             q=step.q[:, j, :], tokens=step.tokens[:, j],
+                             dev_status=step.status[2:3], workspace=step.ws_draft)
+        vt.vt_verify(d["logits"], step.q, step.inv_map, step.tokens, d["u_accept"],
+                     d["u_resample"], T, out_tokens=step.out_tokens,
+                     out_num_accepted=step.out_n, out_accept_prob=step.out_acc,
+                     dev_status=step.status[3:4], workspace=step.ws_ver)
+        done[x].record(stream)
+        out_host[: B * (GAMMA + 1)].copy_(step.out_tokens.view(-1), non_blocking=True)
+        out_host[B * (GAMMA + 1):].copy_(step.out_n, non_blocking=True)
+
+    def pipeline(n):
+        copy_stream.wait_stream(stream)
+        issue_copy(0)
+        for k in range(n):
+            if k + 1 < n:
+                issue_copy(k + 1)
+            run_block(k)
+
+    pipeline(2)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    pipeline(nblocks)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(torch, e0.elapsed_time(e1), dist, dev)
+    # the same blocks with the inputs already on the device (GPU-only time)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for k in range(nblocks):
+        run_block_dev = sets[k % 2]
+        for j in range(GAMMA):
+            vt.vt_draft_step(run_block_dev["hidden"][j], step.W_trim, step.trim_ids,
+                             run_block_dev["u_draft"][j], T, q=step.q[:, j, :],
+                             tokens=step.tokens[:, j], dev_status=step.status[2:3],
+                             workspace=step.ws_draft)
+        vt.vt_verify(run_block_dev["logits"], step.q, step.inv_map, step.tokens,
+                     run_block_dev["u_accept"], run_block_dev["u_resample"], T,
+                     out_tokens=step.out_tokens, out_num_accepted=step.out_n,
+                     out_accept_prob=step.out_acc, dev_status=step.status[3:4],
+                     workspace=step.ws_ver)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_dev = max_over_ranks(torch, e2.elapsed_time(e3), dist, dev)
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    return {"value": whole_job_value(nblocks, world, ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_host.numel() * 4,
+            "blocks": nblocks, "ms_per_block": ms / nblocks,
+            "link_gbs": h2d / (ms / nblocks * 1e-3) / 1e9,
+            "gpu_only": {"value": whole_job_value(nblocks, world, ms_dev), "unit": UNIT,
+                         "ms_per_block": ms_dev / nblocks},
+            "block": "6 drafting steps (B=16) and the verification; calibration and trim "
+                     "offline, W_trim resident",
+            "overlap": "copies of block k+1 on a second stream during block k"}
 
 
 def run_e2e(torch, step, host, stream, args, dist, dev, world):
