@@ -457,6 +457,8 @@ def run_row(torch, vt, dev, host, args):
                                            tokens=step.tokens[:, j],
                                            dev_status=step.status[2:3],
                                            workspace=step.ws_draft) for j in range(GAMMA)],
+        # the drafter's top-8 candidates (the expansion step of a draft tree)
+        "topk": lambda: vt.vt_draft_topk(step.hidden[0], step.W_trim, step.trim_ids, 8, T),
         "verify": lambda: vt.vt_verify(s["logits"], step.q, step.inv_map, step.tokens,
                                        s["u_acc"], s["u_res"], T, out_tokens=step.out_tokens,
                                        out_num_accepted=step.out_n,
@@ -474,8 +476,9 @@ def run_row(torch, vt, dev, host, args):
         fn()
     e1.record()
     torch.cuda.synchronize()
-    per_call = e0.elapsed_time(e1) * 1e3 / (args.steps * CALLS_PER_STEP[args.row])
-    print(json.dumps({"row": args.row, "calls": args.steps * CALLS_PER_STEP[args.row],
+    ncalls = args.steps * CALLS_PER_STEP.get(args.row, 1)
+    per_call = e0.elapsed_time(e1) * 1e3 / ncalls
+    print(json.dumps({"row": args.row, "calls": ncalls,
                       "us_per_call": per_call,
                       "dev_status": [int(v) for v in step.status.cpu().tolist()]}))
     return 0
@@ -491,7 +494,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
-    ap.add_argument("--row", default=None, choices=ROWS,
+    ap.add_argument("--row", default=None, choices=ROWS + ["topk"],
                     help="profiling mode: after one full step, run only this row's calls for "
                          "warmup + steps iterations (prints a short summary, not the bench line)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
@@ -617,6 +620,7 @@ def main():
                       **run_selection(torch, vt, step),
                       "block_graph": run_block_graph(torch, vt, step),
                       "verify_batched": run_verify_batched(torch, vt, step, host),
+                      "toy_chain": run_toy_chain(torch, vt),
                       **run_tree(torch, vt, step)},
     }
     if not args.no_configs:
@@ -1113,6 +1117,93 @@ def run_timing_distribution(torch, vt, step, host, ncalls: int = 240):
                    "costs the launch overlap between calls); graph_per_call: replays of a graph "
                    "of calls, time per call of each replay")
     return out
+
+
+def toy_expectations(p_tab, q_tab, gamma: int):
+    """Exact per-context expectations of the toy workload's blocks
+    ("A rejection rule keeps speculative decoding's output exact", section
+    "What draft accuracy buys"; "Speculative decoding" glossary, "Why a
+    rejection needs a special draw").  A drafted x ~ q(.|c) is accepted with
+    probability min(1, p(x|c)/q(x|c)), so a position with context c is
+    accepted with probability beta(c) = sum_x min(p, q)(x|c), and the
+    accepted token is x with probability min(p, q)(x|c) / beta(c); the next
+    position's context is x + 1 (contexts: 0 = BOS, t + 1 after token t).
+    Returns beta [C] and E[tokens per block | block starts at c] [C] (the
+    accepted drafts plus the one drawn token)."""
+    mn = np.minimum(np.asarray(p_tab, np.float64), np.asarray(q_tab, np.float64))
+    beta = mn.sum(axis=1)
+    acc = np.zeros(mn.shape[0])           # expected accepted drafts, 0 positions left
+    for _ in range(gamma):
+        acc = beta + mn @ acc[1:]         # the next context after token x is x + 1
+    return beta, 1.0 + acc
+
+
+def run_toy_chain(torch, vt, nblocks: int = 50_000, gamma: int = 4, seed: int = 31):
+    """The toy workload (V = 18, 19 contexts, q_w = (p + q0)/2, gamma = 4) as
+    a chain of blocks through vt_verify on the GPU, the drafts drawn on the
+    host from q_w: tau (tokens per block) and the empirical acceptance rate
+    alpha against their exact expectations over the visited contexts."""
+    p_tab, _, q_tab = synthetic.toy_tables()
+    Vt = p_tab.shape[1]
+    beta, etok = toy_expectations(p_tab, q_tab, gamma)
+    logp = torch.from_numpy(np.log(p_tab).astype(np.float32)).cuda()
+    qd = torch.from_numpy(q_tab.astype(np.float32)).cuda()
+    g = synthetic.rng(seed, 0)
+    ua = torch.from_numpy(synthetic.uniforms(seed, 1, (nblocks, gamma))).cuda()
+    ur = torch.from_numpy(synthetic.uniforms(seed, 2, (nblocks, gamma + 1))).cuda()
+    inv_map = torch.arange(Vt, dtype=torch.int32, device="cuda")
+    logits = torch.empty((1, gamma + 1, Vt), dtype=torch.float32, device="cuda")
+    q = torch.empty((1, gamma, Vt), dtype=torch.float32, device="cuda")
+    dr = torch.empty((1, gamma), dtype=torch.int32, device="cuda")
+    ws = torch.empty(vt.workspace_bytes("verify", B=1, gamma=gamma, V=Vt, K=Vt),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty((1, gamma + 1), dtype=torch.int32, device="cuda")
+    n_t = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    ctx = 0
+    status = 0
+    ns = np.empty(nblocks, np.int64)
+    e_tok = np.empty(nblocks)
+    b_sum = b_var = 0.0
+    tested = 0
+    t0 = time.perf_counter()
+    for k in range(nblocks):
+        draft = synthetic.toy_drafts(g, q_tab, ctx, gamma)
+        ctxs = [ctx] + [int(x) + 1 for x in draft]
+        ci = torch.tensor(ctxs, device="cuda")
+        logits[0].copy_(logp[ci])
+        q[0].copy_(qd[ci[:gamma]])
+        dr[0].copy_(torch.from_numpy(draft))
+        vt.vt_verify(logits, q, inv_map, dr, ua[k:k + 1], ur[k:k + 1], 1.0, out_tokens=out,
+                     out_num_accepted=n_t, dev_status=st, workspace=ws,
+                     want_accept_prob=False)
+        res = torch.cat([out[0], n_t, st]).cpu().numpy()
+        n = int(res[gamma + 1])
+        status |= int(res[gamma + 2])
+        ns[k] = n
+        e_tok[k] = etok[ctx]
+        t = min(n + 1, gamma)                 # positions tested in this block
+        bb = beta[np.array(ctxs[:t])]
+        b_sum += float(bb.sum())
+        b_var += float((bb * (1 - bb)).sum())
+        tested += t
+        ctx = int(res[n]) + 1                 # the block's last emitted token
+    wall = time.perf_counter() - t0
+    tau = float((ns + 1).mean())
+    tau_exact = float(e_tok.mean())
+    tau_sigma = float(np.std(ns + 1 - e_tok) / np.sqrt(nblocks))
+    alpha = float(ns.sum() / tested)
+    alpha_exact = b_sum / tested
+    alpha_sigma = float(np.sqrt(b_var) / tested)
+    return {"blocks": nblocks, "gamma": gamma, "dev_status": status,
+            "tau": tau, "tau_exact": tau_exact, "tau_sigma": tau_sigma,
+            "tau_within_4_sigma": abs(tau - tau_exact) <= 4 * tau_sigma,
+            "alpha": alpha, "alpha_exact_mean_beta": alpha_exact, "alpha_sigma": alpha_sigma,
+            "alpha_within_4_sigma": abs(alpha - alpha_exact) <= 4 * alpha_sigma,
+            "tokens_per_block": tau, "wall_s": wall,
+            "note": "drafts from the toy q_w on the host, one vt_verify call per block on "
+                    "the GPU; exact values: per-context expectations of the rule averaged "
+                    "over the visited contexts"}
 
 
 def run_e2e_block(torch, step, host, stream, args, dist, dev, world):

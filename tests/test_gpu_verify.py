@@ -181,8 +181,11 @@ def test_bad_inputs_set_device_status(vt):
 
 def test_toy_chain_exact_and_chi_square(vt):
     """200k chained blocks of the toy (V=18, gamma=4, w=0.5) through the GPU:
-    per-block parity with the oracle on the first 20k blocks, and a chi-square
-    test of every emitted transition against the target chain p."""
+    per-block parity with the oracle on the first 20k blocks, a chi-square
+    test of every emitted transition against the target chain p, and the
+    empirical tokens per block (tau) and acceptance rate (alpha) within 4
+    sigma of their exact expectations over the visited contexts."""
+    import bench
     from scipy import stats
     steps, gamma, parity_steps = 200_000, 4, 20_000
     p_tab, _, q_tab = synthetic.toy_tables()
@@ -210,6 +213,11 @@ def test_toy_chain_exact_and_chi_square(vt):
     rec_tok = np.empty((parity_steps, gamma + 1), np.int32)
     rec_n = np.empty(parity_steps, np.int32)
     counts = np.zeros((V + 1, V), np.int64)
+    beta, etok = bench.toy_expectations(p_tab, q_tab, gamma)
+    ns = np.empty(steps, np.int64)
+    e_tok = np.empty(steps)
+    b_sum = b_var = 0.0
+    tested = 0
     ctx = 0
     status = 0
     for s in range(steps):
@@ -225,6 +233,13 @@ def test_toy_chain_exact_and_chi_square(vt):
         toks = res[: gamma + 1]
         n = int(res[gamma + 1])
         status |= int(res[gamma + 2])
+        ns[s] = n
+        e_tok[s] = etok[ctx]
+        t = min(n + 1, gamma)
+        bb = beta[np.array([ctx] + [int(x) + 1 for x in draft[: t - 1]])]
+        b_sum += float(bb.sum())
+        b_var += float((bb * (1 - bb)).sum())
+        tested += t
         if s < parity_steps:
             rec_ctx[s] = ctx
             rec_draft[s] = draft
@@ -250,6 +265,11 @@ def test_toy_chain_exact_and_chi_square(vt):
         stat += float(((counts[c] - e) ** 2 / e).sum())
         dof += V - 1
     assert stats.chi2.sf(stat, dof) > 1e-3
+    # tau and alpha against the exact expectations of the rule
+    tau, tau_exact = (ns + 1).mean(), e_tok.mean()
+    assert abs(tau - tau_exact) <= 4 * np.std(ns + 1 - e_tok) / np.sqrt(steps)
+    alpha, alpha_exact = ns.sum() / tested, b_sum / tested
+    assert abs(alpha - alpha_exact) <= 4 * np.sqrt(b_var) / tested
 
 
 def test_parity_largest_batch(vt):

@@ -243,3 +243,19 @@ def test_toy_chain_chi_square_rejects_naive_redraw(monkeypatch):
     monkeypatch.setattr(spec, "residual_weights", lambda p, q: np.asarray(p, dtype=np.float64))
     counts, p_tab = _toy_chain(20_000)
     assert _chi2_pvalue(counts, p_tab) < 1e-6
+
+
+def test_toy_expectations_match_enumeration():
+    # bench.toy_expectations (beta per context and the expected tokens per
+    # block of the Markov toy) against the exact block distribution obtained by
+    # enumerating every draft and integrating oracle.verify over its uniforms
+    import bench
+    for V, gamma, seed in [(3, 2, 5), (4, 3, 6)]:
+        p_tab, _, q_tab = synthetic.toy_tables(V=V, w=0.4, seed=seed)
+        beta, etok = bench.toy_expectations(p_tab, q_tab, gamma)
+        for c in range(V + 1):
+            d1 = markov_block_distribution(oracle.verify, p_tab, q_tab, c, 1)
+            acc1 = sum(pr for toks, pr in d1.items() if len(toks) == 2)
+            assert beta[c] == pytest.approx(acc1, abs=1e-12)
+            d = markov_block_distribution(oracle.verify, p_tab, q_tab, c, gamma)
+            assert etok[c] == pytest.approx(sum(pr * len(t) for t, pr in d.items()), abs=1e-12)
