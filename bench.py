@@ -817,11 +817,48 @@ def run_block_graph(torch, vt, step, nblocks: int = 100):
     tau = float((g.out_num_accepted.float() + 1).mean().item())
     status = [int(x) for x in g.dev_status.cpu().tolist()]
     g.close()
+    # Overlap of block k+1's W_trim stream with block k's verification: the
+    # first projection of a block requests its W_trim stages before its
+    # dependency wait, while the verification's finish (which releases its
+    # dependents early) still runs.  Measured two ways:
+    #  - graphs of 20 consecutive blocks against graphs of one block (no
+    #    kernel of the previous replay to overlap);
+    #  - direct blocks back to back against the same with an event recorded
+    #    between blocks (an event between kernels cuts the overlap).
+    sep = torch.cuda.Event()
+
+    def direct_cut():
+        direct()
+        sep.record()
+
+    for name, fn in (("direct_cut", direct_cut),):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(nblocks):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) * 1e3 / nblocks
+    res["graph_of_1"] = graph_us(torch, direct, 1, reps=20)
+    res["graph_of_20"] = graph_us(torch, direct, 20, reps=5)
     return {"value": B * GAMMA / (res["graph"] * 1e-6), "unit": UNIT,
             "us_per_block_graph": res["graph"], "us_per_block_direct": res["direct"],
             "tau": tau, "dev_status": status,
+            "w_trim_overlap": {
+                "us_per_block_graph_of_1": res["graph_of_1"],
+                "us_per_block_graph_of_20": res["graph_of_20"],
+                "us_per_block_direct_cut": res["direct_cut"],
+                "us_per_block_direct": res["direct"],
+                "gain_graph_us": res["graph_of_1"] - res["graph_of_20"],
+                "note": "block k+1's first projection streams W_trim during block k's "
+                        "verification; 'cut': an event between blocks removes the overlap"},
             "note": "drafting steps + verification as one CUDA graph (calibrate/trim excluded); "
-                    "tau = mean tokens per block on the synthetic (unaligned) drafter"}
+                    "tau = mean tokens per block on the synthetic (unaligned) drafter; tau on "
+                    "the toy workload is next_rows.toy_chain"}
 
 
 def run_selection(torch, vt, step, ncalls: int = 20):
