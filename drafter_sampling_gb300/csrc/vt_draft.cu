@@ -238,6 +238,7 @@ struct FinArgs {
   const float2* part;  // [G][B] partials of consecutive row tiles
   int G;
   int tile_rows;       // rows per partial (64 or 128; divides kFinChunk)
+  int passes;          // chunks of kFinChunk ids per CTA
   const float* u;
   const int* trim_ids;
   int* tokens;
@@ -246,15 +247,50 @@ struct FinArgs {
   int vec_ok;
 };
 
-constexpr int kFinChunk = kFinNT * 4;  // ids normalised per CTA
+constexpr int kFinChunk = kFinNT * 4;  // ids normalised per CTA and pass
 
-// Normalises q for one chunk of 1024 ids of row b and, in the CTA whose chunk
-// holds the sampled tile, draws the token.  The projection left one online-
-// softmax partial (m_t, s_t) per tile of consecutive rows; the tile masses
-// s_t 2^(m_t - m) in units of the global 2^m are therefore known to every CTA
-// without waiting on any other: all CTAs of row b scan the tile masses in
-// tile order to find the tile where the running mass passes u_b * S, and the
-// warp holding that tile scans its rows (ascending id) to pick the row.
+// finalize passes per CTA.  A sampling CTA merges all of its row's partials
+// and scans its tile masses whatever its share of the row, so a row is split
+// over few CTAs: at least four passes each, and a grid of at most about 512
+// CTAs (measured on the drafting step for B = 1..256: fewer, longer CTAs
+// were faster down to these bounds).  The greedy finalize only merges the
+// (max, row) partials and writes a one-hot row: up to about 1216 CTAs.
+inline int fin_passes(int B, int K, bool greedy) {
+  const int64_t p1 = (K + kFinChunk - 1) / kFinChunk;  // 1024-id passes per row
+  const int64_t target = greedy ? 1216 : 512;
+  int64_t r = std::max<int64_t>(greedy ? 1 : std::min<int64_t>(4, p1), (p1 * B + target - 1) / target);
+  return (int)std::min(r, p1);
+}
+
+// the passes of one batch: loaded together (RB float4 loads in flight per
+// thread), then weighted, drawn from and stored
+template <int RB>
+__device__ __forceinline__ void fin_load(float (&z)[RB][4], const float* qrow, int64_t j0, int p0,
+                                         int np, int K, bool vec_ok) {
+#pragma unroll
+  for (int q = 0; q < RB; ++q) {
+    const int64_t j = j0 + (int64_t)(p0 + q) * kFinChunk;
+    if (p0 + q < np && vec_ok && j + 3 < K) {
+      const float4 v = *reinterpret_cast<const float4*>(qrow + j);
+      z[q][0] = v.x; z[q][1] = v.y; z[q][2] = v.z; z[q][3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) z[q][e] = (p0 + q < np && j + e < K) ? qrow[j + e] : kNegBig;
+    }
+  }
+}
+
+// Normalises q for a.passes consecutive chunks of 1024 ids of row b and, in
+// the CTA whose chunks hold the sampled tile, draws the token.  The
+// projection left one online-softmax partial (m_t, s_t) per tile of
+// consecutive rows; the global (m, S) and the tile masses s_t 2^(m_t - m) in
+// units of the global 2^m are therefore known to every CTA without waiting
+// on any other: all CTAs of row b scan the tile masses in tile order to find
+// the tile where the running mass passes u_b * S, and the warp holding that
+// tile scans its rows (ascending id) to pick the row.  The chunks are
+// streamed in batches of RB passes (four consecutive ids per thread and
+// pass); the first batch is requested before the partials are merged.
+template <int RB>
 __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   __shared__ MS mred[kFinNT / 32];
   __shared__ float sred[kFinNT / 32];
@@ -270,16 +306,13 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
   griddep_launch_dependents();
   griddep_wait();  // the projection has completed
 
-  // this thread's ids (four consecutive) and tiles (consecutive)
-  const int64_t j = (int64_t)c * kFinChunk + 4 * (int64_t)tid;
-  float z[4];
-  if (a.vec_ok && j + 3 < a.K) {
-    const float4 v = *reinterpret_cast<const float4*>(qrow + j);
-    z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) z[e] = (j + e < a.K) ? qrow[j + e] : kNegBig;
-  }
+  // this CTA's passes [0, np) start at cbase; in pass p this thread holds
+  // ids j0 + p * kFinChunk + [0, 4)
+  const int64_t cbase = (int64_t)c * kFinChunk * a.passes;
+  const int64_t j0 = cbase + 4 * (int64_t)tid;
+  const int np = (int)min((int64_t)a.passes, (a.K - cbase + kFinChunk - 1) / kFinChunk);
+  float z[RB][4];
+  fin_load<RB>(z, qrow, j0, 0, np, a.K, a.vec_ok != 0);
   const int per = (a.G + kFinNT - 1) / kFinNT;
   const int t0 = tid * per, t1 = min(a.G, t0 + per);
   float2 pt[kRegTiles];
@@ -298,9 +331,6 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     return;
   }
   const float m = g.m, invS = 1.f / g.s;
-  float w[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) w[e] = (j + e < a.K) ? exp2_approx(z[e] - m) : 0.f;
   auto tile_part = [&](int t) -> float2 {
     return (t - t0 < kRegTiles) ? pt[t - t0] : a.part[(int64_t)t * a.B + b];
   };
@@ -355,60 +385,82 @@ __global__ void __launch_bounds__(kFinNT) draft_finalize_kernel(FinArgs a) {
     force_last = true;
   }
   const int64_t r0 = (int64_t)max(tsel, 0) * a.tile_rows;
-  const bool owner_cta =
-      tsel >= 0 && r0 >= (int64_t)c * kFinChunk && r0 < (int64_t)(c + 1) * kFinChunk;
-  const int owner_warp = owner_cta ? (int)((r0 - (int64_t)c * kFinChunk) / 4) >> 5 : -1;
-  if ((tid >> 5) == owner_warp) {
-    // this CTA holds the tile: its rows are consecutive threads of one warp
-    const int64_t r1 = min((int64_t)a.K, r0 + a.tile_rows);
-    float v = 0.f;
+  const bool owner_cta = tsel >= 0 && r0 >= cbase && r0 < cbase + (int64_t)kFinChunk * np;
+  // a tile lies within one pass (tile_rows divides kFinChunk)
+  const int opass = owner_cta ? (int)((r0 - cbase) / kFinChunk) : -1;
+  const int owner_warp = owner_cta ? (int)(((r0 - cbase) % kFinChunk) / 4) >> 5 : -1;
+
+#pragma unroll 1
+  for (int p0 = 0; p0 < np; p0 += RB) {
+    if (p0 > 0) fin_load<RB>(z, qrow, j0, p0, np, a.K, a.vec_ok != 0);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j + e >= r0 && j + e < r1) v += w[e];
-    float x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    const float local = target - before;
-    const unsigned hit = force_last ? 0u : __ballot_sync(0xffffffffu, x > local);
-    int pick = -1;
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      if (lane == l) {
-        float acc = x - v;
-        int lastp = -1;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (j + e < r0 || j + e >= r1) continue;
-          if (w[e] > 0.f) lastp = (int)(j + e);
-          acc += w[e];
-          if (pick < 0 && acc > local) pick = (int)(j + e);
-        }
-        if (pick < 0) pick = lastp;
-      }
-      pick = __shfl_sync(0xffffffffu, pick, l);
-    } else {
-      // last row with weight in the tile
-      int lp = -1;
+    for (int q = 0; q < RB; ++q)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (j + e >= r0 && j + e < r1 && w[e] > 0.f) lp = (int)(j + e);
-      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-      pick = lp;
-    }
-    if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
-  }
-
-  // normalise this chunk in place
-  if (a.vec_ok && j + 3 < a.K) {
-    *reinterpret_cast<float4*>(qrow + j) =
-        make_float4(w[0] * invS, w[1] * invS, w[2] * invS, w[3] * invS);
-  } else {
+        z[q][e] = (j0 + (int64_t)(p0 + q) * kFinChunk + e < a.K) ? exp2_approx(z[q][e] - m) : 0.f;
+    if ((tid >> 5) == owner_warp && opass >= p0 && opass < p0 + RB) {
+      // this batch holds the tile: its rows are consecutive threads of one warp
+      const int64_t r1 = min((int64_t)a.K, r0 + a.tile_rows);
+      const int64_t j = j0 + (int64_t)opass * kFinChunk;
+      float w[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j + e < a.K) qrow[j + e] = w[e] * invS;
+      for (int q = 0; q < RB; ++q)
+        if (p0 + q == opass)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) w[e] = z[q][e];
+      float v = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j + e >= r0 && j + e < r1) v += w[e];
+      float x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const float local = target - before;
+      const unsigned hit = force_last ? 0u : __ballot_sync(0xffffffffu, x > local);
+      int pick = -1;
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        if (lane == l) {
+          float acc = x - v;
+          int lastp = -1;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (j + e < r0 || j + e >= r1) continue;
+            if (w[e] > 0.f) lastp = (int)(j + e);
+            acc += w[e];
+            if (pick < 0 && acc > local) pick = (int)(j + e);
+          }
+          if (pick < 0) pick = lastp;
+        }
+        pick = __shfl_sync(0xffffffffu, pick, l);
+      } else {
+        // last row with weight in the tile
+        int lp = -1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e >= r0 && j + e < r1 && w[e] > 0.f) lp = (int)(j + e);
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        pick = lp;
+      }
+      if (lane == 0) a.tokens[(int64_t)b * a.ldt] = (pick >= 0) ? a.trim_ids[pick] : -1;
+    }
+    // normalise this batch in place
+#pragma unroll
+    for (int q = 0; q < RB; ++q) {
+      if (p0 + q >= np) continue;
+      const int64_t j = j0 + (int64_t)(p0 + q) * kFinChunk;
+      if (a.vec_ok && j + 3 < a.K) {
+        *reinterpret_cast<float4*>(qrow + j) =
+            make_float4(z[q][0] * invS, z[q][1] * invS, z[q][2] * invS, z[q][3] * invS);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < a.K) qrow[j + e] = z[q][e] * invS;
+      }
+    }
   }
 }
 
@@ -416,6 +468,7 @@ struct GreedyFinArgs {
   float* q;            // in: raw logits z; out: one-hot at the greedy index
   int64_t ldq;
   int B, K;
+  int passes;          // chunks of kFinChunk ids per CTA
   const float2* part;  // [G][B] (max z, its lowest row) of consecutive row tiles
   int G;
   const int* trim_ids;
@@ -427,8 +480,9 @@ struct GreedyFinArgs {
 
 // Greedy drafting (temperature 0): j* = the largest z of row b, ties to the
 // lower trimmed index, from the projection's per-tile (max, row) partials;
-// q[b, :] = one-hot at j*; token = trim_ids[j*].  Grid (B, chunks of 1024
-// ids): every CTA merges the partials itself and writes its chunk of q.
+// q[b, :] = one-hot at j*; token = trim_ids[j*].  Grid (B, chunks of
+// a.passes x 1024 ids): every CTA merges the partials itself and writes its
+// chunk of q.
 __global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFinArgs a) {
   __shared__ float sv[kFinNT / 32];
   __shared__ int si[kFinNT / 32];
@@ -461,16 +515,19 @@ __global__ void __launch_bounds__(kFinNT) draft_greedy_finalize_kernel(GreedyFin
     }
   const bool ok = (v == v) && idx >= 0 && idx < a.K;  // NaN: a non-finite z was seen
   float* qrow = a.q + (int64_t)b * a.ldq;
-  const int64_t j = (int64_t)c * kFinChunk + 4 * (int64_t)tid;
-  float o[4];
+#pragma unroll 4
+  for (int p = 0; p < a.passes; ++p) {
+    const int64_t j = ((int64_t)c * a.passes + p) * kFinChunk + 4 * (int64_t)tid;
+    float o[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) o[e] = (ok && j + e == idx) ? 1.f : 0.f;
-  if (a.vec_ok && j + 3 < a.K) {
-    *reinterpret_cast<float4*>(qrow + j) = make_float4(o[0], o[1], o[2], o[3]);
-  } else {
+    for (int e = 0; e < 4; ++e) o[e] = (ok && j + e == idx) ? 1.f : 0.f;
+    if (a.vec_ok && j + 3 < a.K) {
+      *reinterpret_cast<float4*>(qrow + j) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j + e < a.K) qrow[j + e] = o[e];
+      for (int e = 0; e < 4; ++e)
+        if (j + e < a.K) qrow[j + e] = o[e];
+    }
   }
   if (c == 0 && tid == 0) {
     a.tokens[(int64_t)b * a.ldt] = ok ? a.trim_ids[idx] : -1;
@@ -859,12 +916,14 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
   // for wide ones (one CTA per SM)
   const int budget = (BN <= 64) ? 96 * 1024 : 200 * 1024;
   a.stages = std::max(2, std::min(umma::kMaxStages, budget / stage));
-  const size_t smem = (size_t)a.stages * stage + 1024;
+  // the ring also holds one transposed accumulator tile in the epilogue
+  constexpr size_t kZt = (size_t)BN * umma::kZtLd * sizeof(float);
+  const size_t smem = std::max((size_t)a.stages * stage, kZt) + 1024;
   auto k = umma::head_umma_kernel<BN, TM>;
   VT_RETURN_IF_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((tiles + TM - 1) / TM));
-  cfg.blockDim = dim3(umma::kThreads);
+  cfg.blockDim = dim3(umma::kHeadThreads<BN>);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1012,8 +1071,10 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
     ga.ldt = ld_tokens;
     ga.dev_status = dev_status;
     ga.vec_ok = ((reinterpret_cast<uintptr_t>(q) & 15) == 0) && (ldq % 4 == 0);
+    const int R = fin_passes(B, K, true);
+    ga.passes = R;
     cudaLaunchConfig_t gcfg = {};
-    gcfg.gridDim = dim3((unsigned)B, (unsigned)((K + kFinChunk - 1) / kFinChunk));
+    gcfg.gridDim = dim3((unsigned)B, (unsigned)((K + kFinChunk * R - 1) / (kFinChunk * R)));
     gcfg.blockDim = dim3(kFinNT);
     gcfg.stream = s;
     cudaLaunchAttribute gattr[1];
@@ -1039,7 +1100,9 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
   fa.ldt = ld_tokens;
   fa.dev_status = dev_status;
   fa.vec_ok = ((reinterpret_cast<uintptr_t>(q) & 15) == 0) && (ldq % 4 == 0);
-  const int nchunk = (K + kFinChunk - 1) / kFinChunk;
+  const int R = fin_passes(B, K, false);
+  fa.passes = R;
+  const int nchunk = (K + kFinChunk * R - 1) / (kFinChunk * R);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B, (unsigned)nchunk);
   cfg.blockDim = dim3(kFinNT);
@@ -1049,7 +1112,9 @@ int vt::draft_step_impl(const uint16_t* hidden, int32_t B, int32_t H, const uint
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, draft_finalize_kernel, fa));
+  auto fk = R == 1 ? draft_finalize_kernel<1>
+            : R == 2 ? draft_finalize_kernel<2> : draft_finalize_kernel<4>;
+  VT_RETURN_IF_CUDA(cudaLaunchKernelEx(&cfg, fk, fa));
   return VT_OK;
 }
 

@@ -35,7 +35,6 @@ constexpr int kBM = 128;            // W_trim rows per tile (MMA M)
 constexpr int kBK = 64;             // reduction elements per stage (128 bytes)
 constexpr int kABytes = kBM * 128;  // one A stage: 128 rows x 128 bytes
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 128;
 // polls of an mbarrier before a wait gives up: an incomplete try_wait
 // suspends for ~3.8 us on sm_103a, so this is about one second, far above
 // any wait of a working pipeline (the longest, the epilogue's wait for the
@@ -174,6 +173,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive fp32 columns of this thread's TMEM lane; the wait is part
+// of the same statement, so no use of the registers can precede it
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// threads of the projection CTA: wide batches (BN >= 128) add a second
+// group of four warps, which reads the other half of the accumulator's
+// columns (the same TMEM lanes) in the epilogue
+template <int BN>
+constexpr int kHeadThreads = BN >= 128 ? 256 : 128;
+
 struct HeadArgs {
   int B, H, K;
   float out_scale;
@@ -209,12 +234,95 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
+constexpr int kZtLd = kBM + 4;  // row pitch (floats) of the transposed tile
+
+// Per-column partials of one accumulator tile held transposed in shared
+// memory (zt[b][r], r < nvalid rows of the tile starting at row r0):
+// sampling, (max z, sum 2^(z - max)); greedy, (max z, its lowest row), a
+// non-finite z counting as NaN, which wins.  P = NT/BN threads share a
+// column (narrow batches), interleaved by 16-byte groups so that a quarter
+// warp reads 32 distinct banks; with BN > NT each thread owns BN/NT columns.
+template <int BN, int NT>
+__device__ __forceinline__ void tile_partials(const float* zt, const HeadArgs& a, int nvalid,
+                                              int r0, int tt, int tid) {
+  constexpr int P = BN >= NT ? 1 : NT / BN;          // threads per column
+  constexpr int CPT = BN > NT ? BN / NT : 1;         // columns per thread
+  constexpr int NF = kBM / 4 / P;                    // 16-byte groups per thread
+  const int p = tid % P;
+#pragma unroll
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int b = tid / P + cc * (NT / P);
+    const float4* col = reinterpret_cast<const float4*>(zt + b * kZtLd);
+    if (a.greedy) {
+      float v = -INFINITY;
+      int idx = 0x7fffffff;
+#pragma unroll 4
+      for (int k = 0; k < NF; ++k) {
+        const int f = p + P * k;
+        const float4 x4 = col[f];
+        const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * f + e;
+          const float w = isfinite(xs[e]) ? xs[e] : __int_as_float(0x7fc00000);
+          if (r < nvalid && argmax_better(v, idx, w, r0 + r)) {
+            v = w;
+            idx = r0 + r;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        const int k = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (argmax_better(v, idx, w, k)) {
+          v = w;
+          idx = k;
+        }
+      }
+      if (p == 0 && b < a.B) a.part[(int64_t)tt * a.B + b] = make_float2(v, __int_as_float(idx));
+    } else {
+      // two passes over the column: its max, then the sum of 2^(z - max);
+      // a NaN or +inf z leaves the sum NaN
+      float m = kNegBig;
+#pragma unroll 4
+      for (int k = 0; k < NF; ++k) {
+        const int f = p + P * k;
+        const float4 x4 = col[f];
+        if (4 * f + 3 < nvalid) {
+          m = fmaxf(m, fmaxf(fmaxf(x4.x, x4.y), fmaxf(x4.z, x4.w)));
+        } else {
+          const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (4 * f + e < nvalid) m = fmaxf(m, xs[e]);
+        }
+      }
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float s = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < NF; ++k) {
+        const int f = p + P * k;
+        const float4 x4 = col[f];
+        const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * f + e < nvalid) s += exp2_approx(xs[e] - m);
+      }
+#pragma unroll
+      for (int o = P / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (p == 0 && b < a.B) a.part[(int64_t)tt * a.B + b] = make_float2(m, s);
+    }
+  }
+}
+
 // one CTA per TM consecutive 128-row tiles of W_trim; BN = padded batch
 // (16..256, step 16).  With TM = 2 the two tiles share every staged block of
 // hidden states (two MMAs per step, one TMEM accumulator each), which halves
 // the hidden-state traffic of wide batches.
 template <int BN, int TM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kHeadThreads<BN>, 1)
 head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                  HeadArgs a) {
   static_assert(TM == 1 || TM == 2, "one or two tiles per CTA");
@@ -230,7 +338,6 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int s_err;
-  __shared__ MS red[4][BN];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
@@ -311,7 +418,7 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   } else {
     griddep_wait();
     if (tile == 0 && warp >= 2) {
-      for (int i = tid - 64; i < a.nzero; i += kThreads - 64) a.zero_ints[i] = 0;
+      for (int i = tid - 64; i < a.nzero; i += kHeadThreads<BN> - 64) a.zero_ints[i] = 0;
       if (tid == 64 && a.status_reset) *a.status = 0;
     }
   }
@@ -343,66 +450,50 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
   }
   __syncwarp();
 
-  // epilogue: all four warps; the next kernel may launch meanwhile
-  const bool acc_ok = mbar_wait(&acc_bar, 0);
+  // epilogue: all four warps; the next kernel may launch meanwhile.  The
+  // threads agree on whether the accumulator is complete, so the barriers
+  // below are reached by all of them or by none.
+  const bool acc_ok = __syncthreads_and(mbar_wait(&acc_bar, 0) ? 1 : 0) != 0;
   griddep_launch_dependents();
   fence_after_sync();
-  const int row = warp * 32 + lane;
+  if (!acc_ok && tid == 0) s_err = 1;
+  constexpr int NT = kHeadThreads<BN>;
+  constexpr int CW = BN / (NT / 128);  // accumulator columns read by one warp group
+  constexpr int CH = CW >= 32 ? 32 : 16;
+  const int quad = warp & 3, col0 = (warp >> 2) * CW;
+  const int row = quad * 32 + lane;  // TMEM lane = row of the tile
+  // Once every MMA has completed the stage ring is idle (each stage was
+  // consumed, so no copy is in flight): it holds one accumulator tile
+  // transposed, zt[column b][row], so that the per-column partials are
+  // reduced by threads that own whole columns rather than by a chain of
+  // warp shuffles per column.
+  float* zt = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-  for (int t = 0; t < TM; ++t) {
+  for (int t = 0; t < TM && acc_ok; ++t) {
     const int j = m0 + t * kBM + row;
     const int tt = tile * TM + t;  // this 128-row tile
-    if (acc_ok) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * BN + c0), v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int b = c0 + e;
-          const float z = v[e] * a.out_scale;
-          if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
-          if (a.part != nullptr && a.greedy) {
-            float v = (j < a.K) ? (isfinite(z) ? z : __int_as_float(0x7fc00000)) : -INFINITY;
-            int idx = (j < a.K) ? j : 0x7fffffff;
-            warp_argmax(v, idx);
-            if (lane == 0) red[warp][b] = MS{v, __int_as_float(idx)};
-          } else if (a.part != nullptr) {
-            MS m = (j < a.K) ? MS{z, 1.f} : MS{kNegBig, 0.f};
-            m = warp_ms_reduce(m);
-            if (lane == 0) red[warp][b] = m;
-          }
-        }
+    for (int c0 = col0; c0 < col0 + CW; c0 += CH) {
+      float v[CH];
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(t * BN + c0);
+      if constexpr (CH == 32) {
+        tmem_ld32(taddr, v);
+      } else {
+        tmem_ld16(taddr, v);
       }
-    } else {
-      atomicExch(&s_err, 1);
+#pragma unroll
+      for (int e = 0; e < CH; ++e) {
+        const int b = c0 + e;
+        const float z = v[e] * a.out_scale;
+        if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
+        if (a.part != nullptr) zt[b * kZtLd + row] = z;
+      }
     }
     fence_before_sync();
     __syncthreads();
-    if (a.part != nullptr && acc_ok && m0 + t * kBM < a.K) {
-      for (int b = tid; b < a.B && b < BN; b += kThreads) {
-        MS r = red[0][b];
-        if (a.greedy) {
-          float v = r.m;
-          int idx = __float_as_int(r.s);
-          for (int w = 1; w < 4; ++w) {
-            const float wv = red[w][b].m;
-            const int wi = __float_as_int(red[w][b].s);
-            if (argmax_better(v, idx, wv, wi)) {
-              v = wv;
-              idx = wi;
-            }
-          }
-          a.part[(int64_t)tt * a.B + b] = make_float2(v, __int_as_float(idx));
-        } else {
-          r = ms_combine(r, red[1][b]);
-          r = ms_combine(r, red[2][b]);
-          r = ms_combine(r, red[3][b]);
-          a.part[(int64_t)tt * a.B + b] = make_float2(r.m, r.s);
-        }
-      }
-    }
-    __syncthreads();  // red is reused by the next tile
+    if (a.part != nullptr && m0 + t * kBM < a.K)
+      tile_partials<BN, NT>(zt, a, min(kBM, a.K - (m0 + t * kBM)), m0 + t * kBM, tt, tid);
+    __syncthreads();  // zt is reused by the next tile
   }
   if (tid == 0 && s_err) atomicOr(a.status, VT_DEV_TIMEOUT);
   if (warp == 1) {
