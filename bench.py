@@ -259,6 +259,11 @@ class GpuStep:
         self.out_n = torch.empty(B, dtype=i32, device=dev)
         self.out_acc = torch.empty((B, GAMMA), dtype=torch.float32, device=dev)
         self.status = torch.zeros(4, dtype=i32, device=dev)
+        # the per-position views a decoder holds for its drafting steps
+        # (hidden states, uniforms, q column, token column), made once
+        self.draft_views = [(self.hidden[j], self.u_draft[j], self.q[:, j, :], self.tokens[:, j])
+                            for j in range(GAMMA)]
+        self.status_views = [self.status[i:i + 1] for i in range(4)]
         u8 = torch.uint8
         self.ws_cal = torch.empty(vt.workspace_bytes("calibrate", n=N_CAL, V=V, K=K), dtype=u8,
                                   device=dev)
@@ -287,26 +292,25 @@ class GpuStep:
                 elif i == 2 * ncalls[row] - 1:
                     group[2].record()
 
+        sv = self.status_views
         mark("calibrate", 0)
         vt.vt_calibrate_topk(self.ids, V, K, counts=self.counts, topk_ids=self.topk,
-                             dev_status=self.status[0:1], workspace=self.ws_cal)
+                             dev_status=sv[0], workspace=self.ws_cal)
         mark("calibrate", 1)
         mark("trim", 0)
         vt.vt_trim_head(self.W, self.topk, W_trim=self.W_trim, trim_ids=self.trim_ids,
-                        inv_map=self.inv_map, dev_status=self.status[1:2],
-                        workspace=self.ws_trim)
+                        inv_map=self.inv_map, dev_status=sv[1], workspace=self.ws_trim)
         mark("trim", 1)
         for j in range(GAMMA):
+            hj, uj, qj, tj = self.draft_views[j]
             mark("draft", 2 * j)
-            vt.vt_draft_step(self.hidden[j], self.W_trim, self.trim_ids, self.u_draft[j], T,
-                             q=self.q[:, j, :], tokens=self.tokens[:, j],
-                             dev_status=self.status[2:3], workspace=self.ws_draft)
+            vt.vt_draft_step(hj, self.W_trim, self.trim_ids, uj, T, q=qj, tokens=tj,
+                             dev_status=sv[2], workspace=self.ws_draft)
             mark("draft", 2 * j + 1)
         mark("verify", 0)
         vt.vt_verify(s["logits"], self.q, self.inv_map, self.tokens, s["u_acc"], s["u_res"], T,
                      out_tokens=self.out_tokens, out_num_accepted=self.out_n,
-                     out_accept_prob=self.out_acc, dev_status=self.status[3:4],
-                     workspace=self.ws_ver)
+                     out_accept_prob=self.out_acc, dev_status=sv[3], workspace=self.ws_ver)
         mark("verify", 1)
 
 

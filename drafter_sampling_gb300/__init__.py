@@ -29,16 +29,32 @@ def lib():
     return _lib.load()
 
 
+_TORCH = None
+_RAW_STREAM = None  # torch's raw current-stream getter, or False where it has none
+_BF16 = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _stream_ptr(stream):
+    """The cudaStream_t of `stream`, or of the current device's current
+    stream (read without building a torch.cuda.Stream object, which costs a
+    few microseconds of host time per call)."""
+    global _RAW_STREAM
     torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _RAW_STREAM is None:
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _RAW_STREAM:
+        return _RAW_STREAM(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev(t, name, dtypes, dim=None):
@@ -57,8 +73,11 @@ def _dev(t, name, dtypes, dim=None):
 
 
 def _bf16_dtypes():
-    torch = _torch()
-    return (torch.bfloat16, torch.int16, torch.uint16)
+    global _BF16
+    if _BF16 is None:
+        torch = _torch()
+        _BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+    return _BF16
 
 
 def _ws(nbytes, device):
