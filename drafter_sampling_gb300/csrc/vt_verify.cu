@@ -59,6 +59,8 @@ struct VArgs {
   int C1;        // stats chunks per row
   int64_t len1;  // ids per stats chunk (multiple of the vector width)
   int C2;        // residual tiles per sequence (kResChunk ids each)
+  int tpc;       // residual tiles per finish CTA (consecutive)
+  int nfin;      // finish CTAs per sequence = ceil(C2 / tpc)
   float2* part;  // [B*R][C1]
   float2* pre;   // [B][gamma]: (scaled logit at x, q(x)); q(x) = -1 if invalid
   float* zpart;  // [B][C2]
@@ -159,26 +161,44 @@ __device__ __forceinline__ void load_kmap(const VArgs& a, int64_t j, int* k) {
   }
 }
 
-// r_e = max(p - q, 0) at ids j..j+7 (zero past V); qrow == nullptr: q = 0
+// the logits at ids j..j+7 of one row (zero past V)
 template <typename T>
-__device__ __forceinline__ void residual8k(const VArgs& a, const T* rowp, const float* qrow,
-                                           int64_t j, float m, float invS, const int* k, float* r) {
-  float x[8];
+__device__ __forceinline__ void load_logits8(const VArgs& a, const T* rowp, int64_t j, float* x) {
   if (a.vec_ok && j + 8 <= a.V) {
     Elem<T>::load8(rowp + j, x);
   } else {
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = (j + e < a.V) ? Elem<T>::load(rowp + j + e) : 0.f;
   }
-  float qv[8];
+}
+
+// q at the trimmed indices k[0..7] (zero where an id is not kept, or
+// qrow == nullptr)
+__device__ __forceinline__ void gather_q8(const VArgs& a, const float* qrow, const int* k,
+                                          float* qv) {
 #pragma unroll
   for (int e = 0; e < 8; ++e)
     qv[e] = (qrow != nullptr && k[e] >= 0 && k[e] < a.K) ? __ldg(qrow + k[e]) : 0.f;
+}
+
+// r_e = max(p - q, 0) at ids j..j+7 from their logits and q (zero past V)
+__device__ __forceinline__ void residual_of(const VArgs& a, const float* x, const float* qv,
+                                            int64_t j, float m, float invS, float* r) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float pj = exp2_approx(x[e] * a.scale - m) * invS;
     r[e] = (j + e < a.V) ? fmaxf(pj - qv[e], 0.f) : 0.f;
   }
+}
+
+// r_e = max(p - q, 0) at ids j..j+7 (zero past V); qrow == nullptr: q = 0
+template <typename T>
+__device__ __forceinline__ void residual8k(const VArgs& a, const T* rowp, const float* qrow,
+                                           int64_t j, float m, float invS, const int* k, float* r) {
+  float x[8], qv[8];
+  load_logits8<T>(a, rowp, j, x);
+  gather_q8(a, qrow, k, qv);
+  residual_of(a, x, qv, j, m, invS, r);
 }
 
 __device__ __forceinline__ float sum8(const float* r) {
@@ -200,6 +220,7 @@ struct Smem {
   int pick;
   int cstar;
   float target;
+  float tsum[2][kNT / 32];  // warp totals of a tile (two alternating slots)
   float zbuf[kResChunk];  // tile sums of one sequence (selection)
 };
 
@@ -250,15 +271,16 @@ __device__ int select_in_tile(const VArgs& a, const T* rowp, const float* qrow, 
 
 // -------------------------------------------------------------- kernel 2
 template <typename T>
-__global__ void __launch_bounds__(kNT, 8) verify_finish_kernel(VArgs a) {
+__global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
   __shared__ Smem sm;
   const int b = blockIdx.x, c = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.R;
+  // this CTA's residual tiles [c0, c1)
+  const int c0 = c * a.tpc, c1 = min(a.C2, c0 + a.tpc);
   // inputs that no earlier kernel of this call writes: fetch before waiting
-  const int64_t jt = (int64_t)c * kResChunk + (int64_t)kResPerThread * tid;
   int kmap[8];
-  load_kmap(a, jt, kmap);
+  load_kmap(a, (int64_t)c0 * kResChunk + (int64_t)kResPerThread * tid, kmap);
   const float ua = (tid < a.gamma) ? a.u_acc[(int64_t)b * a.gamma + tid] : 0.f;
   griddep_wait();  // the stats kernel has completed
 
@@ -323,22 +345,69 @@ __global__ void __launch_bounds__(kNT, 8) verify_finish_kernel(VArgs a) {
     return;
   }
 
-  // 3. residual mass of this tile of row n (p alone at the bonus position)
+  // 3. residual mass of this CTA's tiles of row n (p alone at the bonus
+  // position)
   const T* rowp = static_cast<const T*>(a.logits) + ((int64_t)b * R + n) * a.V;
   const float m_n = sm.m[n];
   const float invS = 1.f / sm.S[n];
   const float* qrow = (n < a.gamma) ? a.q + ((int64_t)b * a.gamma + n) * a.K : nullptr;
   {
-    float r[8], excl, tot;
-    int lp;
-    tile_scan<T>(a, rowp, qrow, (int64_t)c * kResChunk, m_n, invS, kmap, sm, r, excl, tot, lp);
+    // Software pipeline over the CTA's tiles: the next tile's id map and
+    // logits are requested before this tile's residuals are reduced (a
+    // pipeline two tiles deep measured 1-3% slower).  A tile's total takes
+    // the association order of block_scan_incl (warp inclusive scans, then
+    // the warp totals in order), so it equals the total the chosen tile's
+    // rescan computes.  Only the largest positive id over all tiles is
+    // used, so one per CTA is kept.
+    const int64_t jt = (int64_t)kResPerThread * tid;
+    float x[8];
+    load_logits8<T>(a, rowp, (int64_t)c0 * kResChunk + jt, x);
+    int lpmax = -1;
+    for (int ct = c0; ct < c1; ++ct) {
+      const int64_t j = (int64_t)ct * kResChunk + jt;
+      float qv[8];
+      gather_q8(a, qrow, kmap, qv);
+      const bool more = ct + 1 < c1;
+      int kn[8];
+      float xn[8];
+      if (more) {
+        load_kmap(a, j + kResChunk, kn);
+        load_logits8<T>(a, rowp, j + kResChunk, xn);
+      }
+      float r[8];
+      residual_of(a, x, qv, j, m_n, invS, r);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (r[e] > 0.f) lpmax = (int)(j + e);
+      float v = sum8(r);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      float* slot = sm.tsum[ct & 1];
+      if (lane == 31) slot[warp] = v;
+      __syncthreads();
+      if (tid == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNT / 32; ++w) tot += slot[w];
+        a.zpart[(int64_t)b * a.C2 + ct] = tot;
+      }
+      if (more) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kmap[e] = kn[e];
+          x[e] = xn[e];
+        }
+      }
+    }
+    lpmax = block_max_int<kNT>(lpmax, sm.ired);
     griddep_launch_dependents();
-    lp = block_max_int<kNT>(lp, sm.ired);
     if (tid == 0) {
-      a.zpart[(int64_t)b * a.C2 + c] = tot;
-      a.lpart[(int64_t)b * a.C2 + c] = lp;
+      for (int ct = c0; ct < c1; ++ct) a.lpart[(int64_t)b * a.C2 + ct] = lpmax;
       __threadfence();
-      sm.last = (atomicAdd(a.rdone + b, 1u) == (unsigned)(a.C2 - 1));
+      sm.last = (atomicAdd(a.rdone + b, 1u) == (unsigned)(a.nfin - 1));
     }
     __syncthreads();
     if (!sm.last) return;
@@ -433,6 +502,23 @@ struct VerifyLayout {
 
 int chunks2(int64_t V) { return (int)((V + kResChunk - 1) / kResChunk); }
 
+// residual tiles per finish CTA.  Every finish CTA merges its sequence's row
+// partials and replays the accept walk whatever its share of the row, and
+// walks its tiles one after another, so a row is split over few CTAs: the
+// tiles of all rows are dealt out as if to about 608 CTAs (one wave of four
+// 256-thread CTAs per SM).  Measured per verify call in graphs of calls
+// against targets of 304, 1216 and 2432: B = 16 (2 tiles per CTA) 21.8
+// against 23.0-23.9 us, B = 64 57.2 against 60.4-64.5 us, B = 256 (bf16,
+// V = 152064; three CTAs per row, 768 in all) 193 against 196.5-224 us.
+// Splitting rows so that the grid never exceeds one wave was slower at
+// B = 256 (two CTAs per row: 197.7 us).
+void set_finish_split(VArgs& a) {
+  constexpr int64_t kWant = 608;
+  const int64_t t = ((int64_t)a.C2 * a.B + kWant - 1) / kWant;
+  a.tpc = (int)std::max<int64_t>(1, std::min<int64_t>(a.C2, t));
+  a.nfin = (a.C2 + a.tpc - 1) / a.tpc;
+}
+
 VerifyLayout verify_layout(int B, int gamma, int64_t V) {
   VerifyLayout L;
   size_t off = 0;
@@ -470,7 +556,7 @@ template <typename T>
 int launch_verify(const VArgs& a, cudaStream_t s) {
   VT_RETURN_IF_CUDA(launch_pdl(verify_stats_kernel<T>,
                                dim3((unsigned)((int64_t)a.B * a.R), (unsigned)a.C1), s, a));
-  VT_RETURN_IF_CUDA(launch_pdl(verify_finish_kernel<T>, dim3((unsigned)a.B, (unsigned)a.C2), s, a));
+  VT_RETURN_IF_CUDA(launch_pdl(verify_finish_kernel<T>, dim3((unsigned)a.B, (unsigned)a.nfin), s, a));
   return VT_OK;
 }
 
@@ -831,6 +917,7 @@ extern "C" int vt_verify(const void* target_logits, int32_t logits_dtype, int32_
   a.len1 = len1;
   a.C1 = (int)(((int64_t)V + len1 - 1) / len1);
   a.C2 = chunks2(V);
+  set_finish_split(a);
   // 16-byte loads need every row to start on a 16-byte boundary; residual
   // tiles also load inv_map eight ids at a time
   a.vec_ok = ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
@@ -948,6 +1035,7 @@ extern "C" int vt_verify_tree(const void* target_logits, int32_t logits_dtype, i
   a.len1 = len1;
   a.C1 = (int)(((int64_t)V + len1 - 1) / len1);
   a.C2 = chunks2(V);
+  set_finish_split(a);
   a.vec_ok = ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
              (((int64_t)V * esize) % 16 == 0);
   a.part = reinterpret_cast<float2*>(static_cast<char*>(workspace) + L.part);
