@@ -71,6 +71,9 @@ SHAPES = [
     (100, 520, 3001, 0.8),   # padded batch 128: two 128-row tiles per CTA, odd tile count
     (2, 8, 1, 1.0),          # K = 1
     (2, 65536, 64, 1.0),     # the largest hidden size
+    (40, 2048, 9000, 0.1),   # finalize CTAs of four 1024-id passes, the last CTA one ragged pass
+    (200, 1024, 12345, 0.1),  # padded batch 256: two warp groups in the epilogue, six passes
+                             # per finalize CTA, a tile pair whose second tile is past K
 ]
 
 

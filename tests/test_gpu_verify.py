@@ -98,6 +98,8 @@ CASES = [
     (2, 2, 262144, 5000, "f32", 1.0, 1.0),   # a large vocabulary: 128 residual tiles
     (2, 3, 200003, 3000, "bf16", 0.9, 1.0),  # a large ragged vocabulary
     (1, 1, 1 << 22, 4096, "f32", 1.0, 1.0),  # the largest vocabulary: 2048 residual tiles
+    (40, 3, 50000, 4000, "f32", 1.0, 1.0),   # two residual tiles per finish CTA, one left over
+    (300, 3, 70001, 3000, "bf16", 0.8, 0.3),  # 18 and 17 tiles per finish CTA, ragged V
 ]
 
 
