@@ -26,6 +26,7 @@
 //             counts, then tile-local scans that write trim_ids and inv_map),
 //             row gather of W.
 #include <algorithm>
+#include <atomic>
 #include <cooperative_groups.h>
 #include <utility>
 
@@ -883,15 +884,17 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 int num_sms() {
-  static int cache[64] = {0};
+  // per device, filled on first use; concurrent first calls store the same
+  // value (relaxed atomics, so there is no data race)
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 }  // namespace

@@ -283,6 +283,9 @@ __global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
   load_kmap(a, (int64_t)c0 * kResChunk + (int64_t)kResPerThread * tid, kmap);
   const float ua = (tid < a.gamma) ? a.u_acc[(int64_t)b * a.gamma + tid] : 0.f;
   griddep_wait();  // the stats kernel has completed
+  // the drafted tokens' (logit, q) pairs, requested with the partials below
+  float2 pr = make_float2(0.f, -1.f);
+  if (tid < a.gamma) pr = a.pre[(int64_t)b * a.gamma + tid];
 
   // 1. merge the row partials of the gamma+1 rows
   for (int i = warp; i < R; i += kNT / 32) {
@@ -298,8 +301,6 @@ __global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
       sm.S[i] = v.s;
     }
   }
-  float2 pr = make_float2(0.f, -1.f);
-  if (tid < a.gamma) pr = a.pre[(int64_t)b * a.gamma + tid];
   __syncthreads();
 
   // 2. accept walk at every position at once; n = first failing position
