@@ -74,6 +74,7 @@ SHAPES = [
     (40, 2048, 9000, 0.1),   # finalize CTAs of four 1024-id passes, the last CTA one ragged pass
     (200, 1024, 12345, 0.1),  # padded batch 256: two warp groups in the epilogue, six passes
                              # per finalize CTA, a tile pair whose second tile is past K
+    (300, 128, 3000, 0.1),   # B > 256: the CUDA-core projection, three passes per finalize CTA
 ]
 
 

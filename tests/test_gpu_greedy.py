@@ -67,7 +67,8 @@ def _check_greedy_draft(vt, hidden, W, trim_ids, exact_inputs=False):
                                    (33, 96, 777), (64, 512, 2000),
                                    (100, 520, 3001),     # two 128-row tiles per CTA
                                    (256, 128, 1300),     # padded batch 256
-                                   (200, 96, 12345)])    # three passes per finalize CTA
+                                   (200, 96, 12345),     # three passes per finalize CTA
+                                   (300, 64, 2000)])     # B > 256: the CUDA-core projection
 def test_greedy_draft_integer_inputs_bit_exact(vt, B, H, K):
     # small integers: fp32 accumulation is exact, so the argmax is too
     g = synthetic.rng(B + H + K, 3)
