@@ -37,7 +37,7 @@ def _calib(vt, ids, V, K):
     (1000, 50_000, 1, 0.5),         # K = 1
     (70_000, 1_000_001, 5000, 1.1),
     (17, 9, 5, 1.1),                # many zero counts (ties at 0)
-    (300_000, 2_100_000, 20_000, 1.1),  # counts need 22 bits: three sort passes, 37 tiles
+    (300_000, 2_100_000, 20_000, 1.1),  # counts need 22 bits: three sort passes, 74 tiles
     (600_000, 1_000_003, 4096, 1.0),    # V beyond the shared-memory hot-id table
     (1 << 22, 2_000_000, 4096, 1.05),   # the largest vocabulary the sort takes
 ])
@@ -64,7 +64,7 @@ def test_heavy_ties(vt):
 
 
 def test_heavy_ties_many_tiles(vt):
-    # 40000 ids over five sort tiles, counts in {0,..,5}: equal counts span tiles
+    # 40000 ids over twenty sort tiles, counts in {0,..,5}: equal counts span tiles
     g = synthetic.rng(91, 0)
     V = 40_000
     target = g.integers(0, 6, V)
