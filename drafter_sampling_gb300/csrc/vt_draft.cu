@@ -917,7 +917,8 @@ int launch_umma_bn(cudaStream_t s, const CUtensorMap& mw, const CUtensorMap& mh,
   const int budget = (BN <= 64) ? 96 * 1024 : 200 * 1024;
   a.stages = std::max(2, std::min(umma::kMaxStages, budget / stage));
   // the ring also holds one transposed accumulator tile in the epilogue
-  constexpr size_t kZt = (size_t)BN * umma::kZtLd * sizeof(float);
+  constexpr size_t kZt =
+      (size_t)BN * umma::zt_pitch<BN, umma::kHeadThreads<BN>>() * sizeof(float);
   const size_t smem = std::max((size_t)a.stages * stage, kZt) + 1024;
   auto k = umma::head_umma_kernel<BN, TM>;
   VT_RETURN_IF_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));

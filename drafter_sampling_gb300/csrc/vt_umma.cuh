@@ -234,14 +234,23 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-constexpr int kZtLd = kBM + 4;  // row pitch (floats) of the transposed tile
+// Row pitch (floats) of the transposed tile: 128 rows plus 4 P, P = threads
+// sharing a column in the reduction.  The P threads of a column read
+// consecutive 16-byte groups and the next column starts P groups further
+// along the banks, so a quarter warp's eight 16-byte reads hit 32 distinct
+// banks; the row-major writes (one row per lane) are conflict-free at any
+// pitch.
+template <int BN, int NT>
+__host__ __device__ constexpr int zt_pitch() {
+  return kBM + 4 * (BN >= NT ? 1 : NT / BN);
+}
 
 // Per-column partials of one accumulator tile held transposed in shared
 // memory (zt[b][r], r < nvalid rows of the tile starting at row r0):
 // sampling, (max z, sum 2^(z - max)); greedy, (max z, its lowest row), a
 // non-finite z counting as NaN, which wins.  P = NT/BN threads share a
-// column (narrow batches), interleaved by 16-byte groups so that a quarter
-// warp reads 32 distinct banks; with BN > NT each thread owns BN/NT columns.
+// column (narrow batches), interleaved by 16-byte groups (see zt_pitch);
+// with BN > NT each thread owns BN/NT columns.
 template <int BN, int NT>
 __device__ __forceinline__ void tile_partials(const float* zt, const HeadArgs& a, int nvalid,
                                               int r0, int tt, int tid) {
@@ -252,7 +261,7 @@ __device__ __forceinline__ void tile_partials(const float* zt, const HeadArgs& a
 #pragma unroll
   for (int cc = 0; cc < CPT; ++cc) {
     const int b = tid / P + cc * (NT / P);
-    const float4* col = reinterpret_cast<const float4*>(zt + b * kZtLd);
+    const float4* col = reinterpret_cast<const float4*>(zt + b * zt_pitch<BN, NT>());
     if (a.greedy) {
       float v = -INFINITY;
       int idx = 0x7fffffff;
@@ -486,7 +495,7 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
         const int b = c0 + e;
         const float z = v[e] * a.out_scale;
         if (b < a.B && j < a.K) a.out[(int64_t)b * a.ldo + j] = z;
-        if (a.part != nullptr) zt[b * kZtLd + row] = z;
+        if (a.part != nullptr) zt[b * zt_pitch<BN, NT>() + row] = z;
       }
     }
     fence_before_sync();
