@@ -380,12 +380,13 @@ head_umma_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constan
 
   // Everything above overlaps the previous kernel's tail.  The producer also
   // fills the first stages with W_trim tiles before waiting on it: W_trim is
-  // a weight, never written by the kernel just before this one (the kernels
-  // of this library release their dependents only after their own wait, so
-  // every older kernel has completed).  The hidden states join them when the
-  // caller says no running kernel writes them (hidden_ready).  Everything
-  // else -- every output -- waits for the previous kernel
-  // (griddepcontrol.wait).
+  // a weight that no kernel still running writes.  The library's kernels
+  // release their dependents only after their own wait, except the drafting
+  // finalizes, which release on entry; neither they nor the projection
+  // before them write W_trim, and the trim's gather, which does, releases
+  // no dependent early.  The hidden states join them when the caller says
+  // no running kernel writes them (hidden_ready).  Everything else -- every
+  // output -- waits for the previous kernel (griddepcontrol.wait).
   if (warp == 0 && lane == 0) {
     // TMA producer
     const int pre = min(S, nk);

@@ -30,6 +30,14 @@
  *    matching *_workspace_bytes() query returns, 256-byte aligned.  Its
  *    contents need not be initialised.  Two calls that are in flight at the
  *    same time must not share a workspace.
+ *  - Consecutive kernels of the library on one stream overlap through
+ *    programmatic dependent launch: a kernel waits for its predecessor
+ *    before it touches anything an earlier kernel wrote, with one
+ *    exception.  The drafting projection starts streaming W_trim before
+ *    that wait, so W_trim must not be written by a kernel that may still be
+ *    running when the call's first kernel starts: written by vt_trim_head
+ *    (whose last kernel releases no dependent early), by a copy, or by a
+ *    kernel of the caller that does not trigger its dependents early.
  *  - The library holds no random number generator: every uniform the method
  *    draws is an explicit input in [0, 1).
  *  - Device code targets sm_103a only.
