@@ -17,9 +17,10 @@
 //     shared memory (broadcast reads), fp32 FMA accumulation.  Its epilogue
 //     stores z (scaled to base 2 for the softmax) and folds each CTA's rows
 //     into per-row-of-batch online-softmax partials (max, sum 2^(z - max)).
-//  2. draft_finalize grid (B, C): merges the partials, writes q = 2^(z-m)/S
-//     in place; every CTA scans the per-tile masses s_t 2^(m_t - m) in tile
-//     order (no CTA waits on another) to find the tile where the running
+//  2. draft_finalize grid (B, C chunks of several 1024-id passes): merges
+//     the partials, writes q = 2^(z-m)/S in place; every CTA scans the
+//     per-tile masses s_t 2^(m_t - m) in tile order (no CTA waits on
+//     another) to find the tile where the running
 //     mass passes u_b * S, and the CTA holding that tile scans its rows in
 //     ascending id order to pick the token.
 //  Both kernels are launched with programmatic dependent launch: the

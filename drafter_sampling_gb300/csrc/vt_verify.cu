@@ -15,12 +15,13 @@
 //    per chunk, written as a partial.  The first chunk of each drafted row
 //    also gathers the drafted token's scaled logit and its draft probability
 //    q(x), and block (0,0) clears the finish kernel's tickets.
-//  * verify_finish, grid (B, C2 tiles of 2048 ids): merges the row partials,
-//    replays the accept walk for all positions at once (first failing
-//    position = n), sums max(p_n - q_n, 0) over its tile (an L2 re-read of
-//    one row per sequence) and publishes the tile sum.  The last tile of a
-//    sequence to finish (atomic ticket; nothing waits) finds the tile where
-//    the running sum passes u * Z and rescans it to draw the token.
+//  * verify_finish, grid (B, runs of consecutive 2048-id tiles): merges the
+//    row partials, replays the accept walk for all positions at once (first
+//    failing position = n), sums max(p_n - q_n, 0) over each of its tiles
+//    (an L2 re-read of one row per sequence) and publishes the tile sums.
+//    The last CTA of a sequence to finish (atomic ticket; nothing waits)
+//    finds the tile where the running sum passes u * Z and rescans it to
+//    draw the token.
 //  * Both kernels are launched with programmatic dependent launch: each one
 //    waits (griddepcontrol.wait) before touching data an earlier kernel
 //    wrote, and releases its successor near its end, so the successor's
