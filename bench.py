@@ -497,6 +497,42 @@ def run_row(torch, vt, dev, host, args):
     return 0
 
 
+def run_row_large(torch, vt, dev, args):
+    """Profiling mode for the large-batch drafting step (B = 256, H = 4096,
+    K = 38016 trimmed rows, T = 0.7: the tcgen05 tiles of 256 batch columns,
+    two 128-row tiles per CTA): random inputs of those shapes built on the
+    device (about 0.4 GB), then warmup + steps calls."""
+    B4, H4, K4, T4 = 256, 4096, 38016, 0.7
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(21)
+    hidden = torch.randn((B4, H4), generator=gen, device=dev).to(torch.bfloat16)
+    W_trim = (torch.randn((K4, H4), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    trim_ids = torch.arange(K4, dtype=torch.int32, device=dev)
+    u = torch.rand(B4, generator=gen, device=dev)
+    q = torch.empty((B4, K4), dtype=torch.float32, device=dev)
+    tok = torch.empty(B4, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(vt.workspace_bytes("draft", B=B4, H=H4, K=K4), dtype=torch.uint8, device=dev)
+
+    def fn():
+        vt.vt_draft_step(hidden, W_trim, trim_ids, u, T4, q=q, tokens=tok, dev_status=st,
+                         workspace=ws)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"row": args.row, "calls": args.steps,
+                      "us_per_call": e0.elapsed_time(e1) * 1e3 / max(1, args.steps),
+                      "dev_status": int(st.item())}))
+    return 0
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -507,7 +543,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
-    ap.add_argument("--row", default=None, choices=ROWS + ["topk"],
+    ap.add_argument("--row", default=None, choices=ROWS + ["topk", "draft_large"],
                     help="profiling mode: after one full step, run only this row's calls for "
                          "warmup + steps iterations (prints a short summary, not the bench line)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
@@ -532,6 +568,8 @@ def main():
     __graft_entry__.build()
     import drafter_sampling_gb300 as vt
 
+    if args.row == "draft_large":
+        return run_row_large(torch, vt, dev, args)
     host = HostInputs()
     if args.row:
         return run_row(torch, vt, dev, host, args)
