@@ -46,6 +46,7 @@ constexpr int kResPerThread = 8;      // residual ids per thread
 constexpr int kResChunk = kNT * kResPerThread;
 constexpr int kStatsBytes = 32768;    // bytes of logits per stats item
 constexpr int kMaxChunks1 = 64;
+constexpr int kMaxTpc = 64;           // residual tiles per finish CTA at most
 
 struct VArgs {
   const void* logits;
@@ -221,7 +222,7 @@ struct Smem {
   int pick;
   int cstar;
   float target;
-  float tsum[2][kNT / 32];  // warp totals of a tile (two alternating slots)
+  float tsum[kMaxTpc][kNT / 32];  // warp totals of each of the CTA's tiles
   float zbuf[kResChunk];  // tile sums of one sequence (selection)
 };
 
@@ -356,7 +357,9 @@ __global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
   {
     // Software pipeline over the CTA's tiles: the next tile's id map and
     // logits are requested before this tile's residuals are reduced (a
-    // pipeline two tiles deep measured 1-3% slower).  A tile's total takes
+    // pipeline two tiles deep measured 1-3% slower), and no barrier
+    // separates the tiles: each warp keeps its per-tile totals in shared
+    // memory and they are summed after the last tile.  A tile's total takes
     // the association order of block_scan_incl (warp inclusive scans, then
     // the warp totals in order), so it equals the total the chosen tile's
     // rescan computes.  Only the largest positive id over all tiles is
@@ -387,15 +390,9 @@ __global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
         const float y = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += y;
       }
-      float* slot = sm.tsum[ct & 1];
-      if (lane == 31) slot[warp] = v;
-      __syncthreads();
-      if (tid == 0) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNT / 32; ++w) tot += slot[w];
-        a.zpart[(int64_t)b * a.C2 + ct] = tot;
-      }
+      // each warp moves on to the next tile at once: the warp totals are
+      // summed once all tiles are done
+      if (lane == 31) sm.tsum[ct - c0][warp] = v;
       if (more) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -403,6 +400,14 @@ __global__ void __launch_bounds__(kNT, 4) verify_finish_kernel(VArgs a) {
           x[e] = xn[e];
         }
       }
+    }
+    __syncthreads();
+    for (int k = tid; k < c1 - c0; k += kNT) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kNT / 32; ++w) tot += sm.tsum[k][w];
+      a.zpart[(int64_t)b * a.C2 + c0 + k] = tot;
+      __threadfence();  // published before the CTA's ticket below
     }
     lpmax = block_max_int<kNT>(lpmax, sm.ired);
     griddep_launch_dependents();
@@ -517,7 +522,7 @@ int chunks2(int64_t V) { return (int)((V + kResChunk - 1) / kResChunk); }
 void set_finish_split(VArgs& a) {
   constexpr int64_t kWant = 608;
   const int64_t t = ((int64_t)a.C2 * a.B + kWant - 1) / kWant;
-  a.tpc = (int)std::max<int64_t>(1, std::min<int64_t>(a.C2, t));
+  a.tpc = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)a.C2, t, (int64_t)kMaxTpc}));
   a.nfin = (a.C2 + a.tpc - 1) / a.tpc;
 }
 
