@@ -663,7 +663,8 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs (copy, of measured)"},
         "rows": rows,
         "verify_only": {"value": B * GAMMA / (rows["verify"]["avg_call_us_isolated"] * 1e-6),
-                        "unit": UNIT},
+                        "unit": UNIT,
+                        "timing": "one event pair around each call of a short profiling pass"},
         "gpu_launches": sum(KERNELS_PER_CALL[r] * CALLS_PER_STEP[r] for r in ROWS) * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "dev_status": status,
@@ -683,6 +684,13 @@ def main():
             "large_batch_B256": run_large_batch(torch, vt, step, peak, peak_tf)}
 
     line["timing_distribution"] = run_timing_distribution(torch, vt, step, host)
+    # B * gamma / t(vt_verify) with t from graphs of back-to-back calls (no
+    # event between calls), beside the event-pair figure above
+    tv = line["timing_distribution"]["verify"]["graph_per_call"]["median_us"]
+    line["verify_only"]["graph_value"] = B * GAMMA / (tv * 1e-6)
+    line["verify_only"]["graph_us_per_call"] = tv
+    line["verify_only"]["graph_frac_of_measured_hbm"] = \
+        alg["verify"] / (tv * 1e-6) / 1e9 / peak
     if not args.no_e2e:
         line["e2e"] = run_e2e(torch, step, host, stream, args, dist, dev, world)
         line["e2e_online_block"] = run_e2e_block(torch, step, host, stream, args, dist, dev,
